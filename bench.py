@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MLA decode query projection on one GB300.
+
+Workload (one "step"): H = 16 heads, for each weight format / output dtype
+pair (BF16 weights -> BF16 query, MXFP8 weights -> E4M3 query) and each
+token count M in {1, 2, 4, 8, 16, 32}, one replay of a CUDA graph holding
+one fused-query launch per layer over L distinct layers (L = 128 for BF16,
+256 for MXFP8 so that the rotated weights, 256 / 264 MiB, are about twice
+the 126 MiB L2), each launch reading its own weights, q_nope, q_pe and
+writing its own [M,16,576] output.  Launches use programmatic dependent
+launch (weights streamed before the dependency wait), the way consecutive
+layers run in a decode step.
+
+Metric: achieved HBM GB/s = algorithmic bytes (weights + scales + q_nope +
+q_pe + output, per layer call) / time, and microseconds per layer call.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the
+same workload on the host cores (the only other code path this file runs).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+H = 16
+M_POINTS = (1, 2, 4, 8, 16, 32)
+FORMATS = (("bf16", "bf16"), ("mxfp8", "e4m3"))
+DEFAULT_LAYERS = {"bf16": 128, "mxfp8": 256}
+CONFIG_INDEX = {"bf16": 1, "mxfp8": 3}  # seed family 1000*i + layer
+Q_SCALE_SEED = 3
+L2_BYTES = 126 * 2**20
+
+
+def algorithmic_bytes(M, weight_format, out_dtype, h=H):
+    wb = 2 if weight_format == "bf16" else 1
+    ob = 2 if out_dtype == "bf16" else 1
+    scales = h * 128 * 16 if weight_format == "mxfp8" else 0
+    return h * 128 * 512 * wb + scales + 2 * M * h * 128 + 2 * M * h * 64 + M * h * 576 * ob
+
+
+# --------------------------------------------------------------------------- device layer sets
+
+class LayerSet:
+    """L layers of one weight format resident on the GPU, plus per-M input
+    and output buffers laid out [L, M, H, *] so each launch reads its own."""
+
+    def __init__(self, weight_format, out_dtype, n_layers, h=H, m_points=M_POINTS, device="cuda",
+                 config_index=None):
+        import torch
+        from mla_decode_query_gb300 import inputs
+
+        self.weight_format, self.out_dtype, self.L, self.H = weight_format, out_dtype, n_layers, h
+        self.m_points = tuple(m_points)
+        ci = CONFIG_INDEX[weight_format] if config_index is None else config_index
+        self.host = [inputs.make_layer(inputs.layer_seed(ci, l), h, weight_format) for l in range(n_layers)]
+        wdt = torch.int16 if weight_format == "bf16" else torch.uint8
+        w = np.stack([d["weight"] for d in self.host])
+        self.weight = torch.from_numpy(w.view(np.int16) if weight_format == "bf16" else w).to(device)
+        assert self.weight.dtype == wdt
+        self.scale = None
+        if weight_format == "mxfp8":
+            self.scale = torch.from_numpy(np.stack([d["weight_scale"] for d in self.host])).to(device)
+        self.q_scale_value = np.float32(inputs.make_q_scale(Q_SCALE_SEED)) if out_dtype == "e4m3" else None
+        self.q_scale = (torch.tensor([self.q_scale_value], dtype=torch.float32, device=device)
+                        if out_dtype == "e4m3" else None)
+        odt = torch.int16 if out_dtype == "bf16" else torch.uint8
+        self.q_nope_host, self.q_pe_host, self.q_nope, self.q_pe, self.out = {}, {}, {}, {}, {}
+        for M in self.m_points:
+            qn = np.stack([d["q_nope"][:M] for d in self.host]).view(np.int16)
+            qp = np.stack([d["q_pe"][:M] for d in self.host]).view(np.int16)
+            self.q_nope_host[M] = torch.from_numpy(qn).pin_memory()
+            self.q_pe_host[M] = torch.from_numpy(qp).pin_memory()
+            self.q_nope[M] = self.q_nope_host[M].to(device)
+            self.q_pe[M] = self.q_pe_host[M].to(device)
+            self.out[M] = torch.zeros((n_layers, M, h, 576), dtype=odt, device=device)
+
+    def layer_args(self, M, l):
+        return dict(q_nope=self.q_nope[M][l], q_pe=self.q_pe[M][l], weight=self.weight[l],
+                    weight_scale=None if self.scale is None else self.scale[l], out=self.out[M][l],
+                    out_row_stride=576 * self.H, q_scale=self.q_scale, M=M, H=self.H,
+                    weight_format=self.weight_format, out_dtype=self.out_dtype)
+
+    def launch_all(self, M, pdl=True, stream=None):
+        import mla_decode_query_gb300 as mq
+        run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
+        for l in range(self.L):
+            mq.check(run(**self.layer_args(M, l), stream=stream))
+
+    def capture(self, M, pdl=True):
+        import torch
+        import mla_decode_query_gb300 as mq
+        mq.check(mq.mlaqp_prewarm(self.H, max(self.m_points), self.weight_format, self.out_dtype))
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.launch_all(M, pdl, stream=s)  # untimed eager warm-up
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.launch_all(M, pdl)
+        return g
+
+    def bytes_per_call(self, M):
+        return algorithmic_bytes(M, self.weight_format, self.out_dtype, self.H)
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index, self.proc, self.lines = gpu_index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate_over_ranks(local_ms, local_bytes, world_size, backend_device=None):
+    """Whole-job numbers: max time over ranks, sum of bytes over ranks."""
+    if world_size == 1:
+        return local_ms, local_bytes
+    import torch
+    import torch.distributed as dist
+    dev = backend_device or "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    b = torch.tensor([float(local_bytes)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(budget_s, m_points=M_POINTS, layers_per_point=1):
+    """Time the oracle, as it stands, on a bounded sample: one layer call per
+    (format, M) point, repeated until `budget_s` is spent.  Returns
+    (GB/s, calls, seconds)."""
+    import oracle
+    from mla_decode_query_gb300 import inputs
+    samples = []
+    for fmt, od in FORMATS:
+        d = inputs.make_layer(inputs.layer_seed(CONFIG_INDEX[fmt], 0), H, fmt)
+        qs = inputs.make_q_scale(Q_SCALE_SEED) if od == "e4m3" else None
+        samples.append((fmt, od, d, qs))
+    calls, nbytes, t0 = 0, 0, time.perf_counter()
+    while True:
+        for fmt, od, d, qs in samples:
+            for M in m_points:
+                for _ in range(layers_per_point):
+                    oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs)
+                    calls += 1
+                    nbytes += algorithmic_bytes(M, fmt, od)
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return nbytes / el / 1e9, calls, el
+
+
+def oracle_threads():
+    return 1
+
+
+# --------------------------------------------------------------------------- main arms
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        time_oracle(0.0)
+    per_step = []
+    nbytes = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        gbs, calls, el = time_oracle(0.0)
+        per_step.append(el)
+        nbytes += gbs * el * 1e9
+    total = time.perf_counter() - t0
+    value = nbytes / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step": "one oracle layer call per (format, M) point: 12 calls"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
+                         "sample": "per step, one layer call of each of the 12 (format, M) points"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+METRIC = ("achieved HBM GB/s of the fused MLA decode query projection (weights+scales+q_nope+q_pe+out "
+          "bytes per layer call / time), H=16, M in 1..32, BF16 and MXFP8 weights")
+WORKLOAD = ("fused MLA query projection, H=16, K=128, N=512, rope=64; BF16->BF16 and MXFP8->E4M3; "
+            "M in {1,2,4,8,16,32}; 128 (BF16) / 256 (MXFP8) rotated layers per CUDA-graph replay")
+
+
+def run_gpu(args):
+    import torch
+    import mla_decode_query_gb300 as mq
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    mq.load_library()
+
+    m_points = tuple(int(x) for x in args.m.split(",")) if args.m else M_POINTS
+    sets = []
+    for fmt, od in FORMATS:
+        L = args.layers or DEFAULT_LAYERS[fmt]
+        sets.append(LayerSet(fmt, od, L, m_points=m_points))
+    points = [(s, M) for s in sets for M in m_points]
+    graphs = [s.capture(M, pdl=not args.no_pdl) for s, M in points]
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    # untimed warm-up
+    for _ in range(args.warmup):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in points]
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for k in range(args.steps):
+        for i, g in enumerate(graphs):
+            ev[k][i][0].record(stream)
+            g.replay()
+            ev[k][i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    local_ms = t_start.elapsed_time(t_end)
+    step_bytes = sum(s.bytes_per_call(M) * s.L for s, M in points)
+    total_ms, total_bytes = aggregate_over_ranks(local_ms, step_bytes * args.steps, ws,
+                                                 backend_device=f"cuda:{local}")
+    value = total_bytes / (total_ms * 1e-3) / 1e9
+
+    per_point = []
+    kern_ms = {fmt: 0.0 for fmt, _ in FORMATS}
+    kern_bytes = {fmt: 0 for fmt, _ in FORMATS}
+    for i, (s, M) in enumerate(points):
+        ms = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
+        med = statistics.median(ms)
+        us = 1e3 * med / s.L
+        per_point.append({"weights": s.weight_format, "out": s.out_dtype, "M": M, "layers": s.L,
+                          "us_per_layer": round(us, 4),
+                          "gbs": round(s.bytes_per_call(M) / (us * 1e-6) / 1e9, 1)})
+        kern_ms[s.weight_format] += sum(ms)
+        kern_bytes[s.weight_format] += s.bytes_per_call(M) * s.L * args.steps
+
+    # end-to-end through the public API with host buffers
+    e2e = run_e2e(sets, graphs, points, args)
+
+    peaks = load_peaks()
+    launches = args.steps * sum(s.L for s, _ in points)
+    dominant = max(kern_ms, key=kern_ms.get)
+    ach = kern_bytes[dominant] / (kern_ms[dominant] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": f"mlaqp_fused_query_kernel<{dominant} weights>",
+            "achieved": round(ach, 1), "peak": peaks[0], "unit": "GB/s",
+            "frac": round(ach / peaks[0], 4), "peak_source": peaks[1], "traffic": None,
+            "per_kernel_gbs": {f: round(kern_bytes[f] / (kern_ms[f] * 1e-3) / 1e9, 1) for f in kern_ms}}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "heads": H, "m_points": list(m_points),
+                       "layers": {s.weight_format: s.L for s in sets}, "pdl": not args.no_pdl,
+                       "l2": f"rotated weights per replay {[s.L * s.bytes_per_call(1) >> 20 for s in sets]} MiB "
+                             f"vs L2 {L2_BYTES >> 20} MiB (inputs larger than L2, no flush)",
+                       "parallelism": f"replicas{ws}"},
+            "us_per_layer_mean": round(1e3 * total_ms / args.steps / sum(s.L for s, _ in points), 4),
+            "points": per_point,
+            "roofline": roof,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline:
+            gbs, calls, el = time_oracle(args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle_threads(),
+                                    "kind": "oracle",
+                                    "sample": f"{calls} oracle layer calls over the 12 (format, M) points, "
+                                              f"{el:.1f} s, layer 0 of each format"}
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(sets, graphs, points, args):
+    """Same metric through the public API with host buffers: per step, copy
+    every point's q_nope / q_pe from pinned host memory, replay, copy the
+    outputs back to pinned host memory."""
+    import torch
+    stream = torch.cuda.current_stream()
+    host_out = {(id(s), M): torch.empty(s.out[M].shape, dtype=s.out[M].dtype, pin_memory=True) for s, M in points}
+    h2d = sum(s.q_nope_host[M].numel() * 2 + s.q_pe_host[M].numel() * 2 for s, M in points)
+    d2h = sum(s.out[M].numel() * s.out[M].element_size() for s, M in points)
+
+    def step():
+        for (s, M), g in zip(points, graphs):
+            s.q_nope[M].copy_(s.q_nope_host[M], non_blocking=True)
+            s.q_pe[M].copy_(s.q_pe_host[M], non_blocking=True)
+            g.replay()
+            host_out[(id(s), M)].copy_(s.out[M], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    nbytes = sum(s.bytes_per_call(M) * s.L for s, M in points) * args.steps
+    return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms / args.steps, 4)}
+
+
+def load_peaks():
+    p = os.path.join(os.path.dirname(os.path.abspath(__file__)), "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=0, help="override layers per set")
+    ap.add_argument("--m", type=str, default="", help="comma-separated token counts")
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,184 @@
+/*
+ * mlaqp.h -- C ABI of the GB300 (sm_103a) fused MLA decode query projection.
+ *
+ * The operation (SparkInfer PR #75 "Add BF16 MLA query projection and
+ * assembly", sections What and Contract; vLLM PR #174 "Fuse MXFP8 and BF16
+ * MLA query assembly", section What): for every token m < M and head h < H
+ *
+ *   acc[m,h,n] = sum_{k<128} q_nope[m,h,k] * W_UK_T[h,k,n]   (FP32 accumulate)
+ *   out[m,h,n]       = bf16_rne(acc)                        n < 512, BF16 out
+ *                    = e4m3_satfinite(bf16_rne(acc)/q_scale)         E4M3 out
+ *   out[m,h,512+j]   = q_pe[m,h,j]                          j < 64,  BF16 out
+ *                    = e4m3_satfinite(q_pe[m,h,j]/q_scale)           E4M3 out
+ *
+ * in ONE kernel launch: the 64-wide RoPE part is appended by the projection's
+ * epilogue, with no separate concat kernel (vLLM PR #174, section What).
+ * The projection is rounded to BF16 before the optional E4M3 conversion, the
+ * staged operation boundary (SparkInfer PR #75, section Contract).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates, frees or synchronises on the run path.
+ *   - Supported domain (vLLM PR #174, section What: "capability-gated"
+ *     H = 8/11/16 and M = 1..32): num_heads H in {8, 11, 16}, tokens
+ *     1 <= M <= 32, nope dim 128, latent dim 512, rope dim 64, on an
+ *     sm_103 (GB300) device.
+ *   - Status codes are the mlaqp_status values; on any non-OK status a
+ *     message is available from mlaqp_last_error() on the same thread.
+ *
+ * Layouts (row-major, element strides in elements, no padding unless said):
+ *   q_nope        BF16 [M, H, 128]
+ *   q_pe          BF16 [M, H, 64]
+ *   weight        BF16 [H, 128, 512]  (MLAQP_WEIGHT_BF16), latent (N) fastest
+ *                 E4M3 [H, 128, 512]  (MLAQP_WEIGHT_MXFP8), OCP E4M3FN codes
+ *   weight_scale  E8M0 [H, 128, 16]   (MXFP8 only): byte x scales the 32
+ *                 latent elements n in [32*j, 32*j+32) of row (h,k) by
+ *                 2^(x-127) (pages: sf_axis="n", b_major="n"; block size 32
+ *                 along N and the [H,K,N/32] order are this library's
+ *                 reading, the pages give no layout)
+ *   q_scale       one FP32 value in device memory (E4M3 output only), read
+ *                 by the kernel at run time so CUDA-graph replays see
+ *                 updates made between replays
+ *   out           BF16 or E4M3; element (m,h,j), j < 576, is at
+ *                 out[m*out_row_stride + h*576 + j].  Rows >= M and the
+ *                 padding between 576*H and out_row_stride are never written.
+ */
+#ifndef MLAQP_H_
+#define MLAQP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* mlaqp_stream_t;
+
+typedef enum {
+  MLAQP_WEIGHT_BF16 = 0,  /* BF16 W_UK_T                                   */
+  MLAQP_WEIGHT_MXFP8 = 1  /* E4M3 W_UK_T + one E8M0 scale per 32 latent elts */
+} mlaqp_weight_format;
+
+typedef enum {
+  MLAQP_OUT_BF16 = 0,     /* BF16 output; q_scale must be NULL             */
+  MLAQP_OUT_E4M3 = 1      /* E4M3 output scaled by 1/q_scale; q_scale needed */
+} mlaqp_out_dtype;
+
+typedef enum {
+  MLAQP_OK = 0,
+  MLAQP_ERR_UNSUPPORTED = 1,  /* shape, format or device outside the domain */
+  MLAQP_ERR_INVALID_ARG = 2,  /* NULL/misaligned/overlapping pointer, bad
+                                 stride, scale given where it must be absent */
+  MLAQP_ERR_CUDA = 3          /* a CUDA runtime call failed (message kept)  */
+} mlaqp_status;
+
+#define MLAQP_NOPE_DIM 128
+#define MLAQP_LATENT_DIM 512
+#define MLAQP_ROPE_DIM 64
+#define MLAQP_OUT_DIM 576
+#define MLAQP_MAX_M 32
+
+/*
+ * Capability check (SparkInfer PR #75, review of api.py `can_implement`:
+ * num_heads, max_m, nope_dim, latent_dim, output dtype, weight format,
+ * device).  Returns 1 when a call with these sizes, formats and device is
+ * covered, else 0 (and a reason via mlaqp_last_error()).  Launches nothing.
+ * device < 0 means the calling thread's current CUDA device.
+ */
+int mlaqp_can_implement(int num_heads, int max_m, int nope_dim, int latent_dim,
+                        int rope_dim, int weight_format, int out_dtype, int device);
+
+/*
+ * Prewarm (SparkInfer PR #75, walkthrough: the API prewarms weight and M
+ * regimes before the first run; vLLM PR #174, section Layout and topology:
+ * prewarm limited to graph-visible M).  Loads the kernel images of every
+ * specialisation that a run with M <= max_m would use on `device` (< 0:
+ * current), so that later runs -- including runs captured into a CUDA graph
+ * -- trigger no module loading.  Idempotent and thread-safe.  Returns
+ * MLAQP_OK, MLAQP_ERR_UNSUPPORTED or MLAQP_ERR_CUDA.
+ */
+int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, int device);
+
+/*
+ * Run one layer call (SparkInfer PR #75, walkthrough "project q_nope and
+ * append q_pe", "write output tensor").  One kernel launch on `stream`,
+ * asynchronous, no host synchronisation, no allocation: capturable into a
+ * CUDA graph.  Pointer arguments as in the layout table above.
+ *
+ *   weight_scale   required for MLAQP_WEIGHT_MXFP8, must be NULL for BF16
+ *   q_scale        required for MLAQP_OUT_E4M3, must be NULL for BF16 output
+ *                  (vLLM PR #174, section What: "BF16 output omits the unused
+ *                  scale argument"; SparkInfer PR #75, section Contract:
+ *                  "E4M3 output requires one")
+ *   out_row_stride elements between token rows of `out`, >= 576*H, and
+ *                  out_row_stride * element size a multiple of 16 bytes
+ *   M              0 returns MLAQP_OK without launching; 1..32 supported
+ *
+ * Every pointer must be 16-byte aligned (q_scale: 4-byte aligned); the
+ * bytes written to `out` may not overlap any input.  Errors are reported
+ * before anything is launched.
+ */
+int mlaqp_run(const void* q_nope, const void* q_pe, const void* weight,
+              const void* weight_scale, void* out, int64_t out_row_stride,
+              const float* q_scale, int M, int H, int weight_format, int out_dtype,
+              mlaqp_stream_t stream);
+
+/*
+ * As mlaqp_run, but launched with programmatic dependent launch: the kernel
+ * may start while the previous kernel on `stream` is still running, streams
+ * its weights and scales, prefetches the q_nope / q_pe lines into L2, and
+ * only then waits for the previous kernel to finish before it reads q_nope,
+ * q_pe and q_scale or writes `out`.  It also lets the next kernel on the
+ * stream start early.  Use it only when `weight` and `weight_scale` are not
+ * written by the kernel launched immediately before on `stream` (model
+ * weights written once at load time satisfy this).
+ */
+int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
+                  const void* weight_scale, void* out, int64_t out_row_stride,
+                  const float* q_scale, int M, int H, int weight_format, int out_dtype,
+                  mlaqp_stream_t stream);
+
+/*
+ * Launch geometry a run with these arguments uses (for reporting): grid size
+ * in CTAs and threads per CTA.  Returns MLAQP_OK or MLAQP_ERR_UNSUPPORTED.
+ */
+int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas,
+                       int* threads_per_cta);
+
+/*
+ * Device status word (diagnostic, not for the hot path): every in-kernel
+ * wait on a copy-completion barrier is bounded in time; a CTA that gives up
+ * sets MLAQP_DEVSTATUS_WAIT_TIMEOUT here and returns without writing its
+ * part of `out`.  Reads the OR of all bits set on the current device since
+ * the last reset into *status (synchronising with the device); reset != 0
+ * clears it.  Returns MLAQP_OK, MLAQP_ERR_INVALID_ARG or MLAQP_ERR_CUDA.
+ */
+#define MLAQP_DEVSTATUS_WAIT_TIMEOUT 1u
+int mlaqp_device_status(unsigned int* status, int reset);
+
+/*
+ * Test hook for the bounded waits (no counterpart on the pages): as
+ * mlaqp_run, with the wait bound set to wait_limit_ns and the copy barrier
+ * told to expect extra_tx_bytes (<= 2^19) more than the copies deliver, so
+ * that extra_tx_bytes > 0 makes every CTA's wait run out: the kernel then
+ * records MLAQP_DEVSTATUS_WAIT_TIMEOUT, writes nothing and returns.  The
+ * copies themselves complete normally.  Not for production use.
+ */
+int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const void* weight,
+                                 const void* weight_scale, void* out, int64_t out_row_stride,
+                                 const float* q_scale, int M, int H, int weight_format,
+                                 int out_dtype, unsigned long long wait_limit_ns,
+                                 unsigned int extra_tx_bytes, mlaqp_stream_t stream);
+
+/* Message of the last non-OK status returned on this thread ("" if none). */
+const char* mlaqp_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int mlaqp_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MLAQP_H_ */

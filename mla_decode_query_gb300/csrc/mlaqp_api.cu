@@ -1,0 +1,323 @@
+// Host side of the C ABI declared in include/mlaqp.h: argument validation,
+// capability gating, prewarm and the single kernel launch per layer call.
+//
+// The run path allocates nothing, never synchronises and issues exactly one
+// cudaLaunchKernelExC on the caller's stream, so it can be captured into a
+// CUDA graph (SparkInfer PR #75, section Validation: CUDA-graph replay with
+// mutated inputs; vLLM PR #174, section Performance evidence: no extra
+// hot-path synchronisation).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "mlaqp.h"
+#include "mlaqp_dispatch.h"
+#include "mlaqp_kernel.cuh"
+
+namespace {
+
+using mlaqp::KernelInfo;
+using mlaqp::RunParams;
+
+thread_local std::string g_last_error;
+
+int fail(int status, const std::string& msg) {
+  g_last_error = msg;
+  return status;
+}
+
+int fail_cuda(const char* what, cudaError_t e) {
+  return fail(MLAQP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + ": " + cudaGetErrorString(e));
+}
+
+bool supported_heads(int h) { return h == 8 || h == 11 || h == 16; }
+
+constexpr int kMaxDevices = 64;
+// 0 = not yet queried, 1 = sm_103, 2 = another architecture.
+std::atomic<int> g_device_state[kMaxDevices];
+// Bit (wf*2+od)*4 + (mt-1) set once that specialisation's image is loaded.
+std::atomic<uint32_t> g_prewarmed[kMaxDevices];
+std::mutex g_prewarm_mutex;
+
+int resolve_device(int device, int* out) {
+  if (device < 0) {
+    const cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  }
+  if (device >= kMaxDevices) return fail(MLAQP_ERR_UNSUPPORTED, "device ordinal out of range");
+  *out = device;
+  return MLAQP_OK;
+}
+
+// MLAQP_OK if `device` is an sm_103 GPU, else an error status + message.
+int check_device(int device) {
+  int state = g_device_state[device].load(std::memory_order_acquire);
+  if (state == 0) {
+    int major = 0, minor = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute", e);
+    state = (major == 10 && minor == 3) ? 1 : 2;
+    g_device_state[device].store(state, std::memory_order_release);
+  }
+  if (state != 1) return fail(MLAQP_ERR_UNSUPPORTED, "device is not an sm_103 (GB300) GPU");
+  return MLAQP_OK;
+}
+
+// Default bound on every in-kernel mbarrier wait: far above any real copy
+// latency, short enough that a lost completion surfaces as an error.
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library needs no link-time dependency on libcuda.
+EncodeTiledFn encode_tiled_fn(std::string* err) {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  static std::string init_err;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || ptr == nullptr)
+      init_err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(e);
+    else
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  if (!fn) *err = init_err;
+  return fn;
+}
+
+// 2-D tensor map over W_UK_T viewed as [H*128 rows][512 columns]; one box is
+// the 128 x 64 tile a CTA owns.  BF16 tiles land 128B-swizzled (the layout
+// the kernel's ldmatrix addressing expects); E4M3 tiles land unswizzled.
+int encode_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
+  std::string err;
+  EncodeTiledFn fn = encode_tiled_fn(&err);
+  if (!fn) return fail(MLAQP_ERR_CUDA, err);
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM), static_cast<cuuint64_t>(H) * MLAQP_NOPE_DIM};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM) * (mx ? 1 : 2)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(mlaqp::kNTile), static_cast<cuuint32_t>(MLAQP_NOPE_DIM)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(weight), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        mx ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MLAQP_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return MLAQP_OK;
+}
+
+const KernelInfo* lookup(int weight_format, int out_dtype, int M) {
+  const int mt = (M + 7) / 8;
+  if (mt < 1 || mt > 4) return nullptr;
+  const mlaqp::KernelTable& table =
+      weight_format == MLAQP_WEIGHT_BF16 ? mlaqp::kernels_bf16_weights() : mlaqp::kernels_mxfp8_weights();
+  return &table[out_dtype][mt - 1];
+}
+
+bool valid_enums(int weight_format, int out_dtype) {
+  return (weight_format == MLAQP_WEIGHT_BF16 || weight_format == MLAQP_WEIGHT_MXFP8) &&
+         (out_dtype == MLAQP_OUT_BF16 || out_dtype == MLAQP_OUT_E4M3);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+Range span(const void* p, size_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + bytes};
+}
+
+int run_impl(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
+             int64_t out_row_stride, const float* q_scale, int M, int H, int weight_format, int out_dtype,
+             mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
+  if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format or out_dtype");
+  if (M < 0) return fail(MLAQP_ERR_INVALID_ARG, "M must be >= 0");
+  if (!supported_heads(H)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
+  if (M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "M must be <= 32");
+  if (M == 0) return MLAQP_OK;
+
+  const bool mx = weight_format == MLAQP_WEIGHT_MXFP8;
+  const bool e4m3 = out_dtype == MLAQP_OUT_E4M3;
+  if (!q_nope || !q_pe || !weight || !out) return fail(MLAQP_ERR_INVALID_ARG, "q_nope, q_pe, weight and out are required");
+  if (mx && !weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "MXFP8 weights require weight_scale");
+  if (!mx && weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 weights take no weight_scale (pass NULL)");
+  if (e4m3 && !q_scale) return fail(MLAQP_ERR_INVALID_ARG, "E4M3 output requires q_scale");
+  if (!e4m3 && q_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 output takes no q_scale (pass NULL)");
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(weight, 16) || !aligned(out, 16) ||
+      (weight_scale && !aligned(weight_scale, 16)) || (q_scale && !aligned(q_scale, 4)))
+    return fail(MLAQP_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (q_scale 4-byte)");
+  const int64_t out_elem = e4m3 ? 1 : 2;
+  if (out_row_stride < static_cast<int64_t>(MLAQP_OUT_DIM) * H)
+    return fail(MLAQP_ERR_INVALID_ARG, "out_row_stride must be >= 576*H elements");
+  if ((out_row_stride * out_elem) % 16 != 0)
+    return fail(MLAQP_ERR_INVALID_ARG, "out_row_stride * element size must be a multiple of 16 bytes");
+
+  const size_t out_bytes =
+      static_cast<size_t>((static_cast<int64_t>(M - 1) * out_row_stride + static_cast<int64_t>(MLAQP_OUT_DIM) * H) * out_elem);
+  const Range o = span(out, out_bytes);
+  const size_t w_elems = static_cast<size_t>(H) * MLAQP_NOPE_DIM * MLAQP_LATENT_DIM;
+  const Range inputs[5] = {
+      span(q_nope, static_cast<size_t>(M) * H * MLAQP_NOPE_DIM * 2),
+      span(q_pe, static_cast<size_t>(M) * H * MLAQP_ROPE_DIM * 2),
+      span(weight, w_elems * (mx ? 1 : 2)),
+      span(weight_scale, mx ? w_elems / 32 : 0),
+      span(q_scale, e4m3 ? sizeof(float) : 0),
+  };
+  for (const Range& r : inputs)
+    if (r.hi > r.lo && overlaps(o, r)) return fail(MLAQP_ERR_INVALID_ARG, "out overlaps an input tensor");
+
+  int device = 0;
+  int st = resolve_device(-1, &device);
+  if (st != MLAQP_OK) return st;
+  st = check_device(device);
+  if (st != MLAQP_OK) return st;
+
+  const KernelInfo* k = lookup(weight_format, out_dtype, M);
+  RunParams params;
+  st = encode_weight_map(&params.wmap, weight, H, mx);
+  if (st != MLAQP_OK) return st;
+  params.q_nope = static_cast<const uint16_t*>(q_nope);
+  params.q_pe = static_cast<const uint16_t*>(q_pe);
+  params.weight_scale = static_cast<const uint8_t*>(weight_scale);
+  params.out = static_cast<uint8_t*>(out);
+  params.out_row_stride = out_row_stride;
+  params.q_scale = q_scale;
+  params.wait_limit_ns = wait_limit_ns;
+  params.extra_tx = extra_tx;
+  params.M = M;
+  params.H = H;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H), 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(k->smem_bytes);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {&params};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, k->fn, args);
+  if (e != cudaSuccess) return fail_cuda("cudaLaunchKernelExC", e);
+  return MLAQP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlaqp_can_implement(int num_heads, int max_m, int nope_dim, int latent_dim, int rope_dim, int weight_format,
+                        int out_dtype, int device) {
+  if (!valid_enums(weight_format, out_dtype)) return fail(0, "unknown weight_format or out_dtype");
+  if (!supported_heads(num_heads)) return fail(0, "num_heads must be 8, 11 or 16");
+  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(0, "max_m must be in 1..32");
+  if (nope_dim != MLAQP_NOPE_DIM || latent_dim != MLAQP_LATENT_DIM || rope_dim != MLAQP_ROPE_DIM)
+    return fail(0, "only nope_dim=128, latent_dim=512, rope_dim=64 are implemented");
+  int dev = 0;
+  if (resolve_device(device, &dev) != MLAQP_OK) return 0;
+  int count = 0;
+  const cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return fail(0, std::string("no CUDA device: ") + cudaGetErrorString(e));
+  if (dev >= count) return fail(0, "device ordinal out of range");
+  if (check_device(dev) != MLAQP_OK) return 0;
+  return 1;
+}
+
+int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, int device) {
+  if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
+  if (!supported_heads(num_heads)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
+  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "max_m must be in 1..32");
+  int dev = 0;
+  int st = resolve_device(device, &dev);
+  if (st != MLAQP_OK) return st;
+  st = check_device(dev);
+  if (st != MLAQP_OK) return st;
+
+  std::lock_guard<std::mutex> lock(g_prewarm_mutex);
+  int prev = -1;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  if (prev != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return fail_cuda("cudaSetDevice", e);
+  int status = MLAQP_OK;
+  for (int mt = 1; mt <= (max_m + 7) / 8 && status == MLAQP_OK; ++mt) {
+    const uint32_t bit = 1u << (((weight_format * 2 + out_dtype) * 4) + (mt - 1));
+    if (g_prewarmed[dev].load(std::memory_order_acquire) & bit) continue;
+    const KernelInfo* k = lookup(weight_format, out_dtype, 8 * mt);
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, k->fn);  // forces the kernel image to load
+    if (e != cudaSuccess) {
+      status = fail_cuda("cudaFuncGetAttributes", e);
+      break;
+    }
+    g_prewarmed[dev].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  if (prev != dev) cudaSetDevice(prev);
+  return status;
+}
+
+int mlaqp_run(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
+              int64_t out_row_stride, const float* q_scale, int M, int H, int weight_format, int out_dtype,
+              mlaqp_stream_t stream) {
+  return run_impl(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H, weight_format, out_dtype,
+                  stream, false, kDefaultWaitLimitNs, 0);
+}
+
+int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
+                  int64_t out_row_stride, const float* q_scale, int M, int H, int weight_format, int out_dtype,
+                  mlaqp_stream_t stream) {
+  return run_impl(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H, weight_format, out_dtype,
+                  stream, true, kDefaultWaitLimitNs, 0);
+}
+
+int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas, int* threads_per_cta) {
+  if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
+  if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
+  const KernelInfo* k = lookup(weight_format, out_dtype, M);
+  if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
+  if (threads_per_cta) *threads_per_cta = k->threads;
+  return MLAQP_OK;
+}
+
+int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale,
+                                 void* out, int64_t out_row_stride, const float* q_scale, int M, int H,
+                                 int weight_format, int out_dtype, unsigned long long wait_limit_ns,
+                                 unsigned int extra_tx_bytes, mlaqp_stream_t stream) {
+  if (wait_limit_ns == 0) return fail(MLAQP_ERR_INVALID_ARG, "wait_limit_ns must be > 0");
+  if (extra_tx_bytes > (1u << 19)) return fail(MLAQP_ERR_INVALID_ARG, "extra_tx_bytes must be <= 2^19");
+  return run_impl(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H, weight_format, out_dtype,
+                  stream, false, wait_limit_ns, extra_tx_bytes);
+}
+
+int mlaqp_device_status(unsigned int* status, int reset) {
+  if (!status) return fail(MLAQP_ERR_INVALID_ARG, "status must not be NULL");
+  unsigned int a = 0, b = 0;
+  cudaError_t e = mlaqp::device_status_bf16_weights(&a, reset != 0);
+  if (e == cudaSuccess) e = mlaqp::device_status_mxfp8_weights(&b, reset != 0);
+  if (e != cudaSuccess) return fail_cuda("reading the device status word", e);
+  *status = a | b;
+  return MLAQP_OK;
+}
+
+const char* mlaqp_last_error(void) { return g_last_error.c_str(); }
+
+int mlaqp_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,26 @@
+// Internal kernel registry shared by the host-side C ABI and the
+// per-weight-format instantiation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace mlaqp {
+
+struct KernelInfo {
+  const void* fn;      // __global__ function, launched with one RunParams argument
+  int threads;         // threads per CTA
+  int tiles_per_head;  // CTAs per head along the latent axis (grid.x)
+  int smem_bytes;      // dynamic shared memory per CTA
+};
+
+// Table [out_dtype][mt-1], mt = ceil(M/8) in 1..4.
+using KernelTable = KernelInfo[2][4];
+
+const KernelTable& kernels_bf16_weights();
+const KernelTable& kernels_mxfp8_weights();
+
+// Device status word of each instantiation unit (current device).
+cudaError_t device_status_bf16_weights(unsigned int* value, bool reset);
+cudaError_t device_status_mxfp8_weights(unsigned int* value, bool reset);
+
+}  // namespace mlaqp

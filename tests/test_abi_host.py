@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads and exports what include/mlaqp.h declares;
+host-side argument validation returns the documented status codes before
+any CUDA call (no GPU needed)."""
+
+import subprocess
+
+import pytest
+
+import mla_decode_query_gb300 as mq
+from mla_decode_query_gb300 import build
+
+A = 1 << 20  # a 16-byte aligned fake device address, never dereferenced
+H, M = 16, 4
+STRIDE = 576 * H
+
+
+def test_every_declared_symbol_is_exported(built_library):
+    declared = mq.header_functions()
+    assert {"mlaqp_can_implement", "mlaqp_prewarm", "mlaqp_run", "mlaqp_last_error"} <= set(declared)
+    for name in declared:
+        assert hasattr(built_library, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", str(build.LIB_PATH)], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = {line.split()[-1] for line in nm.stdout.splitlines() if line.strip()}
+        assert set(declared) <= exported, set(declared) - exported
+
+
+def test_library_is_built_for_sm103a(built_library):
+    assert "compute_103a,code=sm_103a" in " ".join(build.ARCH_FLAGS)
+    assert mq.mlaqp_version() == 100
+
+
+def _args(**kw):
+    a = dict(q_nope=A, q_pe=2 * A, weight=4 * A, weight_scale=None, out=16 * A, out_row_stride=STRIDE,
+             q_scale=None, M=M, H=H, weight_format="bf16", out_dtype="bf16", stream=0)
+    a.update(kw)
+    return a
+
+
+def _run(**kw):
+    return mq.mlaqp_run(**_args(**kw))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(weight_format=7), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(out_dtype=-1), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(M=-1), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(H=12), mq.MLAQP_ERR_UNSUPPORTED),
+    (dict(H=32), mq.MLAQP_ERR_UNSUPPORTED),
+    (dict(M=33), mq.MLAQP_ERR_UNSUPPORTED),
+    (dict(q_nope=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(q_pe=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(weight=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(out=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(weight_scale=8 * A), mq.MLAQP_ERR_INVALID_ARG),              # BF16 takes no scale
+    (dict(weight_format="mxfp8"), mq.MLAQP_ERR_INVALID_ARG),           # MXFP8 needs a scale
+    (dict(q_scale=32 * A), mq.MLAQP_ERR_INVALID_ARG),                  # BF16 output takes none
+    (dict(out_dtype="e4m3"), mq.MLAQP_ERR_INVALID_ARG),                # E4M3 output needs one
+    (dict(q_nope=A + 8), mq.MLAQP_ERR_INVALID_ARG),                    # misaligned
+    (dict(out=16 * A + 4), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(out_dtype="e4m3", q_scale=32 * A + 2), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(out_row_stride=STRIDE - 8), mq.MLAQP_ERR_INVALID_ARG),       # < 576*H
+    (dict(out_row_stride=STRIDE + 4), mq.MLAQP_ERR_INVALID_ARG),       # 8 bytes, not 16
+    (dict(out=A + 4096), mq.MLAQP_ERR_INVALID_ARG),                    # overlaps q_nope
+    (dict(out=4 * A), mq.MLAQP_ERR_INVALID_ARG),                       # overlaps the weights
+])
+def test_validation_status_codes(built_library, kw, code):
+    assert _run(**kw) == code
+    assert mq.mlaqp_last_error() != ""
+
+
+def test_e4m3_stride_must_be_16_byte_multiple(built_library):
+    # 576*11 E4M3 bytes = 6336 = 16*396 is fine; +8 elements is not.
+    a = dict(H=11, out_row_stride=576 * 11 + 8, out_dtype="e4m3", q_scale=32 * A)
+    assert _run(**a) == mq.MLAQP_ERR_INVALID_ARG
+
+
+def test_zero_tokens_is_a_no_op(built_library):
+    assert _run(M=0, q_nope=None, out=None) == mq.MLAQP_OK
+
+
+def test_valid_arguments_reach_the_device_check(built_library):
+    import torch
+    st = _run()
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    assert st == mq.MLAQP_ERR_CUDA
+    assert mq.mlaqp_can_implement(16, 32) == 0
+
+
+def test_can_implement_domain(built_library):
+    # Shape gating is decided before the device is queried.
+    for bad in [dict(num_heads=12), dict(max_m=0), dict(max_m=33), dict(nope_dim=192),
+                dict(latent_dim=256), dict(rope_dim=32), dict(weight_format=5)]:
+        a = dict(num_heads=16, max_m=32)
+        a.update(bad)
+        assert mq.mlaqp_can_implement(**a) == 0, bad
+
+
+def test_launch_shape(built_library):
+    for h in (8, 11, 16):
+        for m in (1, 9, 32):
+            st, grid, threads = mq.mlaqp_launch_shape(m, h, "mxfp8", "e4m3")
+            assert st == mq.MLAQP_OK and grid == 8 * h and threads == 128
+    assert mq.mlaqp_launch_shape(0, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
+    assert mq.mlaqp_launch_shape(4, 12)[0] == mq.MLAQP_ERR_UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from mla_decode_query_gb300 import mlaqp
+    monkeypatch.setattr(mlaqp, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        mlaqp.load_library(tmp_path / "libmlaqp.so")
