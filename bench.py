@@ -270,12 +270,18 @@ def run_gpu(args):
     mq.load_library()
 
     m_points = tuple(int(x) for x in args.m.split(",")) if args.m else M_POINTS
+    formats = [f for f in FORMATS if not args.formats or f[0] in args.formats.split(",")]
+    if args.pairs:  # explicit weight:output pairs, e.g. bf16:e4m3
+        formats = [tuple(x.split(":")) for x in args.pairs.split(",")]
     sets = []
-    for fmt, od in FORMATS:
+    for fmt, od in formats:
         L = args.layers or DEFAULT_LAYERS[fmt]
         sets.append(LayerSet(fmt, od, L, m_points=m_points))
     points = [(s, M) for s in sets for M in m_points]
     graphs = [s.capture(M, pdl=not args.no_pdl) for s, M in points]
+    alt = None
+    if args.compare_no_pdl and not args.no_pdl:
+        alt = [s.capture(M, pdl=False) for s, M in points]
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -312,8 +318,8 @@ def run_gpu(args):
     value = total_bytes / (total_ms * 1e-3) / 1e9
 
     per_point = []
-    kern_ms = {fmt: 0.0 for fmt, _ in FORMATS}
-    kern_bytes = {fmt: 0 for fmt, _ in FORMATS}
+    kern_ms = {f"{fmt}->{od}": 0.0 for fmt, od in formats}
+    kern_bytes = {f"{fmt}->{od}": 0 for fmt, od in formats}
     for i, (s, M) in enumerate(points):
         ms = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
         med = statistics.median(ms)
@@ -321,17 +327,30 @@ def run_gpu(args):
         per_point.append({"weights": s.weight_format, "out": s.out_dtype, "M": M, "layers": s.L,
                           "us_per_layer": round(us, 4),
                           "gbs": round(s.bytes_per_call(M) / (us * 1e-6) / 1e9, 1)})
-        kern_ms[s.weight_format] += sum(ms)
-        kern_bytes[s.weight_format] += s.bytes_per_call(M) * s.L * args.steps
+        key = f"{s.weight_format}->{s.out_dtype}"
+        kern_ms[key] += sum(ms)
+        kern_bytes[key] += s.bytes_per_call(M) * s.L * args.steps
+
+    if alt is not None:  # context: the same graphs launched without PDL (plain stream order)
+        for i, (s, M) in enumerate(points):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(args.warmup):
+                alt[i].replay()
+            a.record(stream)
+            for _ in range(args.steps):
+                alt[i].replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            per_point[i]["us_per_layer_no_pdl"] = round(1e3 * a.elapsed_time(b) / args.steps / s.L, 4)
 
     # end-to-end through the public API with host buffers
-    e2e = run_e2e(sets, graphs, points, args)
+    e2e = None if args.no_e2e else run_e2e(sets, graphs, points, args)
 
     peaks = load_peaks()
     launches = args.steps * sum(s.L for s, _ in points)
     dominant = max(kern_ms, key=kern_ms.get)
     ach = kern_bytes[dominant] / (kern_ms[dominant] * 1e-3) / 1e9
-    roof = {"bound": "hbm", "kernel": f"mlaqp_fused_query_kernel<{dominant} weights>",
+    roof = {"bound": "hbm", "kernel": f"mlaqp_fused_query_kernel ({dominant})",
             "achieved": round(ach, 1), "peak": peaks[0], "unit": "GB/s",
             "frac": round(ach / peaks[0], 4), "peak_source": peaks[1], "traffic": None,
             "per_kernel_gbs": {f: round(kern_bytes[f] / (kern_ms[f] * 1e-3) / 1e9, 1) for f in kern_ms}}
@@ -413,7 +432,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=0, help="override layers per set")
     ap.add_argument("--m", type=str, default="", help="comma-separated token counts")
+    ap.add_argument("--formats", type=str, default="", help="comma-separated subset of bf16,mxfp8")
+    ap.add_argument("--pairs", type=str, default="", help="comma-separated weight:output pairs, e.g. bf16:e4m3")
     ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--compare-no-pdl", action="store_true", help="also time the graphs without PDL")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     args = ap.parse_args(argv)

@@ -116,12 +116,28 @@ int encode_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
   return MLAQP_OK;
 }
 
-const KernelInfo* lookup(int weight_format, int out_dtype, int M) {
+// Where a PDL-launched CTA lets the next kernel start (see the kernel),
+// chosen from per-layer times of 128-layer CUDA-graph chains on GB300:
+// BF16 weights stream fast enough that triggering after the dependency wait
+// (two kernels in flight, CTAs spread over distinct SMs) wins at every M;
+// MXFP8 tiles need their copy and dequantisation ahead of the wait, so small
+// M triggers at entry (deep overlap) and large M, whose heavier epilogue
+// suffers when CTAs of early-launched kernels share SMs, after the wait.
+int trigger_policy(int weight_format, int mt) {
+  if (weight_format == MLAQP_WEIGHT_BF16) return 1;
+  return mt <= 2 ? 0 : 1;
+}
+
+const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig) {
   const int mt = (M + 7) / 8;
   if (mt < 1 || mt > 4) return nullptr;
   const mlaqp::KernelTable& table =
       weight_format == MLAQP_WEIGHT_BF16 ? mlaqp::kernels_bf16_weights() : mlaqp::kernels_mxfp8_weights();
-  return &table[out_dtype][mt - 1];
+  return &table[out_dtype][mt - 1][trig];
+}
+
+const KernelInfo* lookup(int weight_format, int out_dtype, int M) {
+  return lookup(weight_format, out_dtype, M, trigger_policy(weight_format, (M + 7) / 8));
 }
 
 bool valid_enums(int weight_format, int out_dtype) {
@@ -260,13 +276,13 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
   for (int mt = 1; mt <= (max_m + 7) / 8 && status == MLAQP_OK; ++mt) {
     const uint32_t bit = 1u << (((weight_format * 2 + out_dtype) * 4) + (mt - 1));
     if (g_prewarmed[dev].load(std::memory_order_acquire) & bit) continue;
-    const KernelInfo* k = lookup(weight_format, out_dtype, 8 * mt);
-    cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, k->fn);  // forces the kernel image to load
-    if (e != cudaSuccess) {
-      status = fail_cuda("cudaFuncGetAttributes", e);
-      break;
+    for (int trig = 0; trig < mlaqp::kTrigVariants && status == MLAQP_OK; ++trig) {
+      const KernelInfo* k = lookup(weight_format, out_dtype, 8 * mt, trig);
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, k->fn);  // forces the kernel image to load
+      if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
     }
+    if (status != MLAQP_OK) break;
     g_prewarmed[dev].fetch_or(bit, std::memory_order_acq_rel);
   }
   if (prev != dev) cudaSetDevice(prev);

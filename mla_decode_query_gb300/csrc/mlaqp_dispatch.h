@@ -13,8 +13,11 @@ struct KernelInfo {
   int smem_bytes;      // dynamic shared memory per CTA
 };
 
-// Table [out_dtype][mt-1], mt = ceil(M/8) in 1..4.
-using KernelTable = KernelInfo[2][4];
+// Table [out_dtype][mt-1][trig], mt = ceil(M/8) in 1..4, trig = where the
+// CTA triggers the next kernel's launch (0: at entry, 1: after the
+// dependency wait, 2: once its weight tile is ready).
+constexpr int kTrigVariants = 3;
+using KernelTable = KernelInfo[2][4][kTrigVariants];
 
 const KernelTable& kernels_bf16_weights();
 const KernelTable& kernels_mxfp8_weights();

@@ -58,7 +58,9 @@ constexpr int kTilesPerHead = kLatent / kNTile;  // 8
 constexpr int kSmemA = 0;                            // BF16 [128][64], 128B swizzle: 16 KB
 constexpr int kSmemRaw = kSmemA + kNope * kNTile * 2;  // E4M3 [128][64]: 8 KB
 constexpr int kSmemScale = kSmemRaw + kNope * kNTile;  // E8M0 [128][16]: 2 KB
-constexpr int kSmemBar = kSmemScale + kNope * (kLatent / kMxBlock);
+constexpr int kSmemQ = kSmemScale + kNope * (kLatent / kMxBlock);  // BF16 [32][128], 16B chunks XOR-swizzled: 8 KB
+constexpr int kSmemDiv = kSmemQ + kMaxM * kNope * 2;  // FP32 [128]: RN((128+f)/q_scale)
+constexpr int kSmemBar = kSmemDiv + 128 * 4;
 constexpr int kSmemBytes = kSmemBar + 64 + 1024;  // + slack for the 1024-byte alignment
 
 enum WeightFormat : int { kWeightBF16 = 0, kWeightMXFP8 = 1 };
@@ -177,6 +179,13 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -229,10 +238,73 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair16, float& lo, float&
   asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(h_hi));
 }
 
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// E4M3 codes in bytes 0 and 1 of `two` -> BF16x2 bit patterns of
+// code * 2^-120 (byte 0 in the low half).  The E4M3 exponent and mantissa
+// land in the low bits of the BF16 exponent and the high bits of its
+// mantissa, so every code -- subnormals included -- maps to exactly its
+// value times 2^(7-127).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two) {
+  const uint32_t spread = __byte_perm(two, 0u, 0x4140);  // [b0, 0, b1, 0] -> lanes b0, b1
+  return ((spread & 0x007F007Fu) << 4) | ((spread & 0x00800080u) << 8);
+}
+
+// 2^(x-7) as a BF16 bit pattern, for an E8M0 byte x <= 134 (exponent field
+// x + 120 stays below 255).
+__device__ __forceinline__ uint32_t pow2_bf16(uint32_t x) { return (x + 120u) << 7; }
+
 // E8M0 byte -> 2^(x-127) as FP32 (x = 0 is the subnormal 2^-127, 255 NaN).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t x) {
   const uint32_t bits = x == 0 ? 0x00400000u : (x == 255 ? 0x7FC00000u : (x << 23));
   return __uint_as_float(bits);
+}
+
+// a / q_scale for a BF16 value `a` (bits), as far as the E4M3 conversion
+// that follows can tell: the result converts to the same E4M3 code as the
+// exact IEEE binary32 quotient RN(a / q_scale).  Uses the CTA's table
+// tab[f] = RN((128+f) / q_scale).  A normal BF16 value is (128+f) * 2^(E-134)
+// with f its 7 mantissa bits and E its exponent field, and rounding commutes
+// with scaling by a power of two while the result stays a normal float, so
+// RN(a / q_scale) = tab[f] * 2^(E-134): one exponent add.  Requires
+// 2^-100 <= q_scale <= 2^100, which makes every other case one of
+//   zero or subnormal a, or a result below 2^-126  -> +-0   (E4M3 +-0),
+//   infinite a, or a result of 2^128 or more       -> +-inf (E4M3 +-448),
+//   NaN a                                           -> NaN.
+__device__ __forceinline__ float div_by_table(uint32_t a16, const uint32_t* tab) {
+  const uint32_t e = (a16 >> 7) & 0xFFu;
+  const uint32_t sign = (a16 & 0x8000u) << 16;
+  const uint32_t t = tab[a16 & 0x7Fu];
+  const int er = static_cast<int>(t >> 23) + static_cast<int>(e) - 134;
+  uint32_t r = t + ((e - 134u) << 23);
+  r = (er <= 0 || e == 0u) ? 0u : r;
+  r = (er >= 255 || e == 0xFFu) ? 0x7F800000u : r;
+  r = (e == 0xFFu && (a16 & 0x7Fu)) ? 0x7FC00000u : r;
+  return __uint_as_float(r | sign);
+}
+
+// Plain IEEE division for q_scale outside the table's range (kept out of
+// line: it is not on the common path).
+static __device__ __noinline__ uint32_t e4m3_pair_divide(uint32_t two_bf16, float qs) {
+  return pack_e4m3x2(__fdiv_rn(bf16_hi(two_bf16), qs), __fdiv_rn(bf16_lo(two_bf16), qs));
+}
+
+// Two BF16 values (packed) -> two E4M3 codes (packed, low value in byte 0)
+// of value / q_scale: IEEE division, then saturating RNE conversion.
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t two_bf16, const uint32_t* tab, float qs, bool table_ok) {
+  if (!table_ok) return e4m3_pair_divide(two_bf16, qs);
+  return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..15) of token row `m` in the
+// q_nope tile of 256-byte rows; XOR with m mod 8 makes the eight rows an
+// ldmatrix reads hit eight different bank groups.
+__device__ __forceinline__ uint32_t q_off(int m, int chunk) {
+  return static_cast<uint32_t>(m * 256 + ((chunk ^ (m & 7)) << 4));
 }
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a tile of 128-byte
@@ -243,9 +315,13 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 
 // ---------------------------------------------------------------------------
 // The kernel.  MT = number of 8-token column tiles, ceil(M/8) in 1..4.
+// TRIG selects where the CTA lets the next kernel on the stream launch:
+//   0 = at entry (deepest overlap; the next kernels' CTAs fill free SM slots),
+//   1 = right after the dependency wait (at most two kernels in flight),
+//   2 = once its weight tile is in shared memory (MXFP8: dequantised).
 // ---------------------------------------------------------------------------
 
-template <int WF, int OD, int MT>
+template <int WF, int OD, int MT, int TRIG>
 __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __grid_constant__ RunParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -264,7 +340,7 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
   const int n_cta = tile * kNTile;
 
   // The next kernel on the stream may start its independent prologue.
-  pdl_launch_dependents();
+  if constexpr (TRIG == 0) pdl_launch_dependents();
 
   // 1. Weight (and scale) stream: one elected thread, one barrier phase.
   if (tid == 0) {
@@ -309,76 +385,120 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
     for (int i = 0; i < 8; ++i) {
       const int k = (tid >> 3) + 16 * i;
       const uint2 v = *reinterpret_cast<const uint2*>(raw + k * kNTile + 8 * c);
-      const float f = e8m0_to_f32(sc[k * (kLatent / kMxBlock) + blk]);
+      const uint32_t x = sc[k * (kLatent / kMxBlock) + blk];
+      // value = code * 2^(x-127) = (code * 2^-120) * 2^(x-7), split in two
+      // exact power-of-two factors when 2^(x-7) exceeds BF16's range.
+      const uint32_t s1 = pow2_bf16(min(x, 134u));
+      const uint32_t f1 = s1 | (s1 << 16);
       uint32_t o[4];
       const uint32_t w[2] = {v.x, v.y};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float lo, hi;
-        e4m3x2_to_f32(w[q >> 1] >> (16 * (q & 1)), lo, hi);
-        o[q] = pack_bf16x2(__fmul_rn(hi, f), __fmul_rn(lo, f));
+      for (int q = 0; q < 4; ++q) o[q] = mul_bf16x2(e4m3x2_to_bf16x2_scaled(w[q >> 1] >> (16 * (q & 1))), f1);
+      if (x > 134u) {
+        const uint32_t s2 = x == 255u ? 0x7FC0u : pow2_bf16(x - 127u);  // 2^(x-134)
+        const uint32_t f2 = s2 | (s2 << 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = mul_bf16x2(o[q], f2);
       }
       *reinterpret_cast<uint4*>(smem + kSmemA + sw128(k, c)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     __syncthreads();
+    if constexpr (TRIG == 2) pdl_launch_dependents();
+  } else if constexpr (TRIG == 2) {
+    const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      return;
+    }
+    pdl_launch_dependents();
   }
 
   // 4. Wait for the producer of q_nope / q_pe / q_scale (no-op without PDL).
   pdl_wait();
+  if constexpr (TRIG == 1) pdl_launch_dependents();
 
-  // 5. B fragments: b0 = q[m][16s+2t .. +1], b1 = q[m][16s+8+2t .. +1],
-  //    m = 8*jt + g (zero for m >= M).
-  uint32_t bfrag[MT][8][2];
+  // 5. Inputs: this head's q_nope rows [8*MT][128] (16-byte loads, rows >= M
+  //    zero), this thread's q_pe chunk (if any) and q_scale, all issued back
+  //    to back; then the weight fragments, which need no input.
+  // q_pe chunk (8 elements) of this thread: the head's M*8 chunks are dealt
+  // round-robin to its 8 CTAs and, inside a CTA, to every 4th thread, so
+  // every CTA and warp gets an equal share (at most one chunk per thread).
+  const int nchunks_pe = M * (kRope / 8);
+  const int c_pe = (tid & 3) == 0 ? tile + kTilesPerHead * (tid >> 2) : nchunks_pe;
+  uint4 pe = make_uint4(0u, 0u, 0u, 0u);
+  if (c_pe < nchunks_pe) pe = ld_u128(p.q_pe + (static_cast<size_t>(c_pe >> 3) * H + h) * kRope + 8 * (c_pe & 7));
+  uint4 qv[MT];
 #pragma unroll
-  for (int jt = 0; jt < MT; ++jt) {
-    const int m = 8 * jt + g;
-    if (m < M) {
-      const uint16_t* q = p.q_nope + (static_cast<size_t>(m) * H + h) * kNope + 2 * t;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        bfrag[jt][s][0] = ld_u32(q + 16 * s);
-        bfrag[jt][s][1] = ld_u32(q + 16 * s + 8);
-      }
-    } else {
-#pragma unroll
-      for (int s = 0; s < 8; ++s) bfrag[jt][s][0] = bfrag[jt][s][1] = 0u;
-    }
+  for (int i = 0; i < MT; ++i) {
+    const int c = tid + kThreads * i;  // chunk c: token row c/16, k chunk c%16
+    const int m = c >> 4;
+    qv[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M) qv[i] = ld_u128(p.q_nope + (static_cast<size_t>(m) * H + h) * kNope + 8 * (c & 15));
   }
   float qs = 1.f;
   if constexpr (OD == kOutE4M3) qs = *p.q_scale;
 
-  if constexpr (WF == kWeightBF16) {
+  if constexpr (WF == kWeightBF16 && TRIG != 2) {
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
-    if (__any_sync(0xFFFFFFFFu, !ok)) {
-      if (lane == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
       return;
     }
   }
-
-  // 6. Contraction.  Lane L addresses row (L & 7) of 8x8 matrix L >> 3:
-  //    matrices 0/1 = k 16s..16s+7, 2/3 = k 16s+8..+15; 0/2 = columns
-  //    16w..16w+7, 1/3 = 16w+8..+15 -- the A fragment order of m16n8k16.
-  float acc[MT][4];
-#pragma unroll
-  for (int jt = 0; jt < MT; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.f;
+  // A fragments (weights, transposed by ldmatrix.trans) for all 8 k-steps:
+  // lane L addresses row L&7 of matrix L>>3 -- matrices 0/1 = k 16s..+7,
+  // 2/3 = k 16s+8..+15; 0/2 = columns 16w..+7, 1/3 = 16w+8..+15.
   const int mi = lane >> 3;
   const int chunk = 2 * warp + (mi & 1);
+  uint32_t a[8][4];
 #pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const int k = 16 * s + 8 * (mi >> 1) + (lane & 7);
-    uint32_t a[4];
-    ldmatrix_x4_trans(a, s_a + sw128(k, chunk));
-#pragma unroll
-    for (int jt = 0; jt < MT; ++jt) mma_bf16_16816(acc[jt], a, bfrag[jt][s][0], bfrag[jt][s][1]);
+  for (int s = 0; s < 8; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
+
+  // E4M3 output: table of RN((128+f)/q_scale), one entry per thread.
+  uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + kSmemDiv);
+  bool table_ok = false;
+  if constexpr (OD == kOutE4M3) {
+    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
+    if (table_ok) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
   }
+#pragma unroll
+  for (int i = 0; i < MT; ++i) {
+    const int c = tid + kThreads * i;
+    *reinterpret_cast<uint4*>(smem + kSmemQ + q_off(c >> 4, c & 15)) = qv[i];
+  }
+  __syncthreads();
+
+  // 6. Contraction, two independent accumulator chains (even / odd k-steps).
+  //    B (q_nope): matrix L>>3 of ldmatrix is k chunk 2s2*2 + (L>>3) of tokens
+  //    8jt..8jt+7, giving b0/b1 of steps 2*s2 and 2*s2+1.
+  const uint32_t s_q = smem_u32(smem + kSmemQ);
+  uint32_t b[4][MT][4];
+#pragma unroll
+  for (int s2 = 0; s2 < 4; ++s2)
+#pragma unroll
+    for (int jt = 0; jt < MT; ++jt) ldmatrix_x4(b[s2][jt], s_q + q_off(8 * jt + (lane & 7), 4 * s2 + mi));
+  float acc[2][MT][4];
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+    for (int jt = 0; jt < MT; ++jt) acc[c2][jt][0] = acc[c2][jt][1] = acc[c2][jt][2] = acc[c2][jt][3] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+#pragma unroll
+    for (int jt = 0; jt < MT; ++jt)
+      mma_bf16_16816(acc[s & 1][jt], a[s], b[s >> 1][jt][2 * (s & 1)], b[s >> 1][jt][2 * (s & 1) + 1]);
+#pragma unroll
+  for (int jt = 0; jt < MT; ++jt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[0][jt][e] += acc[1][jt][e];
 
   // 7. Epilogue.  D rows g / g+8 are columns n_cta+16w+g / +8, columns 2t,
   //    2t+1 are tokens.  After movmatrix.trans a lane holds token 8jt+g and
   //    columns 16w+2t, +1 (first block) and 16w+8+2t, +1 (second block).
 #pragma unroll
   for (int jt = 0; jt < MT; ++jt) {
-    const uint32_t r0 = movmatrix_trans(pack_bf16x2(acc[jt][1], acc[jt][0]));
-    const uint32_t r1 = movmatrix_trans(pack_bf16x2(acc[jt][3], acc[jt][2]));
+    const uint32_t r0 = movmatrix_trans(pack_bf16x2(acc[0][jt][1], acc[0][jt][0]));
+    const uint32_t r1 = movmatrix_trans(pack_bf16x2(acc[0][jt][3], acc[0][jt][2]));
     const int m = 8 * jt + g;
     if (m < M) {
       const size_t off =
@@ -389,33 +509,26 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
         *reinterpret_cast<uint32_t*>(o + 8) = r1;
       } else {
         uint8_t* o = p.out + off;
-        *reinterpret_cast<uint16_t*>(o) =
-            static_cast<uint16_t>(pack_e4m3x2(__fdiv_rn(bf16_hi(r0), qs), __fdiv_rn(bf16_lo(r0), qs)));
-        *reinterpret_cast<uint16_t*>(o + 8) =
-            static_cast<uint16_t>(pack_e4m3x2(__fdiv_rn(bf16_hi(r1), qs), __fdiv_rn(bf16_lo(r1), qs)));
+        *reinterpret_cast<uint16_t*>(o) = static_cast<uint16_t>(e4m3_pair(r0, divtab, qs, table_ok));
+        *reinterpret_cast<uint16_t*>(o + 8) = static_cast<uint16_t>(e4m3_pair(r1, divtab, qs, table_ok));
       }
     }
   }
 
-  // 8. Append q_pe: 16-byte chunks (8 elements) spread over the head's CTAs.
-  const int nchunks = M * (kRope / 8);
-  for (int c = tile * kThreads + tid; c < nchunks; c += kTilesPerHead * kThreads) {
-    const int m = c >> 3;
-    const int part = c & 7;
-    const uint4 x = ld_u128(p.q_pe + (static_cast<size_t>(m) * H + h) * kRope + 8 * part);
+  // 8. Append q_pe (chunk loaded right after the dependency wait).
+  if (c_pe < nchunks_pe) {
+    const int m = c_pe >> 3;
+    const int part = c_pe & 7;
     const size_t off =
         static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + kLatent + 8 * part;
     if constexpr (OD == kOutBF16) {
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + off) = x;
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + off) = pe;
     } else {
-      const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+      const uint32_t in[4] = {pe.x, pe.y, pe.z, pe.w};
       uint32_t w[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const uint32_t a = in[2 * i], b = in[2 * i + 1];
-        const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_hi(a), qs), __fdiv_rn(bf16_lo(a), qs));
-        const uint32_t hi = pack_e4m3x2(__fdiv_rn(bf16_hi(b), qs), __fdiv_rn(bf16_lo(b), qs));
-        w[i] = lo | (hi << 16);
+        w[i] = e4m3_pair(in[2 * i], divtab, qs, table_ok) | (e4m3_pair(in[2 * i + 1], divtab, qs, table_ok) << 16);
       }
       *reinterpret_cast<uint2*>(p.out + off) = make_uint2(w[0], w[1]);
     }

@@ -6,17 +6,25 @@ namespace mlaqp {
 namespace {
 constexpr int kWF = kWeightBF16;
 
-template <int OD, int MT>
+template <int OD, int MT, int TRIG>
 KernelInfo entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT>), kThreads,
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT, TRIG>), kThreads,
                     kTilesPerHead, kSmemBytes};
 }
+
+
 }  // namespace
 
 const KernelTable& kernels_bf16_weights() {
   static const KernelTable table = {
-      {entry<kOutBF16, 1>(), entry<kOutBF16, 2>(), entry<kOutBF16, 3>(), entry<kOutBF16, 4>()},
-      {entry<kOutE4M3, 1>(), entry<kOutE4M3, 2>(), entry<kOutE4M3, 3>(), entry<kOutE4M3, 4>()},
+      {{entry<kOutBF16, 1, 0>(), entry<kOutBF16, 1, 1>(), entry<kOutBF16, 1, 2>()},
+       {entry<kOutBF16, 2, 0>(), entry<kOutBF16, 2, 1>(), entry<kOutBF16, 2, 2>()},
+       {entry<kOutBF16, 3, 0>(), entry<kOutBF16, 3, 1>(), entry<kOutBF16, 3, 2>()},
+       {entry<kOutBF16, 4, 0>(), entry<kOutBF16, 4, 1>(), entry<kOutBF16, 4, 2>()}},
+      {{entry<kOutE4M3, 1, 0>(), entry<kOutE4M3, 1, 1>(), entry<kOutE4M3, 1, 2>()},
+       {entry<kOutE4M3, 2, 0>(), entry<kOutE4M3, 2, 1>(), entry<kOutE4M3, 2, 2>()},
+       {entry<kOutE4M3, 3, 0>(), entry<kOutE4M3, 3, 1>(), entry<kOutE4M3, 3, 2>()},
+       {entry<kOutE4M3, 4, 0>(), entry<kOutE4M3, 4, 1>(), entry<kOutE4M3, 4, 2>()}},
   };
   return table;
 }

@@ -182,3 +182,28 @@ def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device):
         _check(d, 4, 8, fmt, "bf16", where="after timeout")  # context still works
         st, word = mq.mlaqp_device_status(reset=False)
         assert word == 0
+
+
+@pytest.mark.parametrize("qs", [0.01, 0.0371, 0.1, 3.0, 1e-20, 1e20, 2.0 ** -110, 2.0 ** 110])
+def test_e4m3_division_every_bf16_value(cuda_device, qs):
+    # The q_pe columns of an E4M3 output are e4m3_satfinite(q_pe / q_scale):
+    # feed every non-NaN BF16 bit pattern through them and require the codes
+    # bit for bit.  The scales cover the kernel's exact table path, results
+    # that overflow or underflow binary32, and q_scale outside 2^-100..2^100
+    # (plain division).
+    H, M = 16, 32
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # drop inf / NaN patterns
+    per_call = M * H * 64
+    qs = np.float32(qs)
+    d = inputs.make_layer(3, H, "bf16", m_max=M)
+    for start in range(0, bits.size, per_call):
+        chunk = bits[start:start + per_call]
+        pe = np.zeros(per_call, dtype=np.uint16)
+        pe[:chunk.size] = chunk
+        pe = pe.reshape(M, H, 64)
+        dd = dict(d, q_pe=pe)
+        got = _rows(_run(_dev_layer(dd, "cuda"), M, H, "bf16", "e4m3", qs), M, H, D * H, "e4m3")
+        with np.errstate(all="ignore"):
+            ref = oracle.f32_to_e4m3_satfinite(oracle.bf16_to_f32(pe) / qs)
+        np.testing.assert_array_equal(got[..., 512:], ref, err_msg=f"q_scale={qs} chunk {start}")
