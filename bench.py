@@ -194,25 +194,29 @@ def aggregate_over_ranks(local_ms, local_bytes, world_size, backend_device=None)
 
 # --------------------------------------------------------------------------- CPU oracle timing
 
-def time_oracle(budget_s, m_points=M_POINTS, layers_per_point=1):
-    """Time the oracle, as it stands, on a bounded sample: one layer call per
-    (format, M) point, repeated until `budget_s` is spent.  Returns
-    (GB/s, calls, seconds)."""
-    import oracle
+def oracle_samples():
+    """One layer of each format (layer 0 of its rotated set), host bits."""
     from mla_decode_query_gb300 import inputs
     samples = []
     for fmt, od in FORMATS:
         d = inputs.make_layer(inputs.layer_seed(CONFIG_INDEX[fmt], 0), H, fmt)
         qs = inputs.make_q_scale(Q_SCALE_SEED) if od == "e4m3" else None
         samples.append((fmt, od, d, qs))
+    return samples
+
+
+def time_oracle(budget_s, samples, m_points=M_POINTS):
+    """Time the oracle, as it stands, on a bounded sample: one layer call per
+    (format, M) point, repeated until `budget_s` is spent (at least once).
+    Returns (GB/s, calls, seconds)."""
+    import oracle
     calls, nbytes, t0 = 0, 0, time.perf_counter()
     while True:
         for fmt, od, d, qs in samples:
             for M in m_points:
-                for _ in range(layers_per_point):
-                    oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs)
-                    calls += 1
-                    nbytes += algorithmic_bytes(M, fmt, od)
+                oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs)
+                calls += 1
+                nbytes += algorithmic_bytes(M, fmt, od)
         el = time.perf_counter() - t0
         if el >= budget_s:
             return nbytes / el / 1e9, calls, el
@@ -228,16 +232,14 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
+    samples = oracle_samples()
     for _ in range(args.warmup):
-        time_oracle(0.0)
-    per_step = []
-    nbytes = 0
-    t0 = time.perf_counter()
+        time_oracle(0.0, samples)
+    nbytes, total = 0.0, 0.0
     for _ in range(args.steps):
-        gbs, calls, el = time_oracle(0.0)
-        per_step.append(el)
+        gbs, calls, el = time_oracle(0.0, samples)
+        total += el
         nbytes += gbs * el * 1e9
-    total = time.perf_counter() - t0
     value = nbytes / total / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -372,7 +374,7 @@ def run_gpu(args):
             "e2e": e2e,
         }
         if not args.no_cpu_baseline:
-            gbs, calls, el = time_oracle(args.cpu_budget)
+            gbs, calls, el = time_oracle(args.cpu_budget, oracle_samples())
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle_threads(),
                                     "kind": "oracle",
                                     "sample": f"{calls} oracle layer calls over the 12 (format, M) points, "

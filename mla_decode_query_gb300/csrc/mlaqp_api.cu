@@ -120,12 +120,12 @@ int encode_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
 // chosen from per-layer times of 128-layer CUDA-graph chains on GB300:
 // BF16 weights stream fast enough that triggering after the dependency wait
 // (two kernels in flight, CTAs spread over distinct SMs) wins at every M;
-// MXFP8 tiles need their copy and dequantisation ahead of the wait, so small
-// M triggers at entry (deep overlap) and large M, whose heavier epilogue
-// suffers when CTAs of early-launched kernels share SMs, after the wait.
+// MXFP8 tiles need their copy and dequantisation ahead of the wait, so M <= 8
+// triggers at entry (deep overlap); larger M, whose heavier epilogue suffers
+// when CTAs of early-launched kernels share SMs, triggers after the wait.
 int trigger_policy(int weight_format, int mt) {
   if (weight_format == MLAQP_WEIGHT_BF16) return 1;
-  return mt <= 2 ? 0 : 1;
+  return mt == 1 ? 0 : 1;
 }
 
 const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig) {
