@@ -127,12 +127,13 @@ int mlaqp_run(const void* q_nope, const void* q_pe, const void* weight,
 /*
  * As mlaqp_run, but launched with programmatic dependent launch: the kernel
  * may start while the previous kernel on `stream` is still running, streams
- * its weights and scales, prefetches the q_nope / q_pe lines into L2, and
- * only then waits for the previous kernel to finish before it reads q_nope,
- * q_pe and q_scale or writes `out`.  It also lets the next kernel on the
- * stream start early.  Use it only when `weight` and `weight_scale` are not
- * written by the kernel launched immediately before on `stream` (model
- * weights written once at load time satisfy this).
+ * its weights and scales, reads q_scale, prefetches the q_nope / q_pe lines
+ * into L2, and only then waits for the previous kernel to finish before it
+ * reads q_nope and q_pe or writes `out`.  It also lets the next kernel on
+ * the stream start early.  Use it only when `weight`, `weight_scale` and
+ * `q_scale` are not written by the kernel launched immediately before on
+ * `stream` (model weights and per-tensor scales written at load time, or by
+ * host copies between graph replays, satisfy this).
  */
 int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
                   const void* weight_scale, void* out, int64_t out_row_stride,

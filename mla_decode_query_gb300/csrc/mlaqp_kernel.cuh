@@ -16,20 +16,24 @@
 //     (BF16: straight into a 128B-swizzled BF16 tile; MXFP8: the E4M3 bytes
 //     plus a 1-D bulk copy of the head's 2 KB of E8M0 scales);
 //  2. warp 0 warms L2 with the head's q_nope / q_pe rows (prefetch only);
+//     q_scale is read (a per-tensor constant, like the weights);
 //  3. MXFP8: all threads wait for the copy and dequantise into the same
-//     swizzled BF16 tile (e4m3 * 2^(e8m0-127), exact);
+//     swizzled BF16 tile (e4m3 * 2^(e8m0-127), exact); E4M3 output: each
+//     thread adds one entry to the exact division table (see div_by_table);
 //  4. griddepcontrol.wait -- everything above is independent of the
 //     previous kernel, so under programmatic dependent launch it overlaps
 //     that kernel; everything below reads inputs it may have produced;
-//  5. q_nope fragments straight from global memory into registers;
-//  6. ldmatrix.trans of the weight fragments, mma.sync m16n8k16 BF16 -> FP32
-//     with the latent axis on the MMA's M side and tokens on its N side
-//     (swap-AB: M <= 32 tokens costs at most four 8-wide column tiles);
+//  5. q_nope rows into a swizzled smem tile (16-byte loads), q_pe pairs into
+//     registers, the weight fragments with ldmatrix.trans;
+//  8. q_pe appended (bit copy or E4M3 cast), one value pair per thread,
+//     ahead of the contraction so that it overlaps the MMA latency;
+//  6. mma.sync m16n8k16 BF16 -> FP32 with the latent axis on the MMA's M
+//     side and tokens on its N side (swap-AB: M <= 32 tokens costs at most
+//     four 8-wide column tiles);
 //  7. epilogue: round to BF16 (optionally divide by q_scale and convert to
 //     E4M3 with saturation), transpose the 8x8 blocks with movmatrix so
 //     each lane holds consecutive latent columns of one token, and store
-//     straight into the caller's strided workspace; q_pe is appended by the
-//     head's CTAs in 16-byte chunks.
+//     straight into the caller's strided workspace.
 //
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
 // records MLAQP_DEVSTATUS_WAIT_TIMEOUT in a device status word and returns
@@ -270,21 +274,23 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t x) {
 // tab[f] = RN((128+f) / q_scale).  A normal BF16 value is (128+f) * 2^(E-134)
 // with f its 7 mantissa bits and E its exponent field, and rounding commutes
 // with scaling by a power of two while the result stays a normal float, so
-// RN(a / q_scale) = tab[f] * 2^(E-134): one exponent add.  Requires
-// 2^-100 <= q_scale <= 2^100, which makes every other case one of
-//   zero or subnormal a, or a result below 2^-126  -> +-0   (E4M3 +-0),
-//   infinite a, or a result of 2^128 or more       -> +-inf (E4M3 +-448),
-//   NaN a                                           -> NaN.
+// RN(a / q_scale) = tab[f] * 2^(E-134): one multiply by a power of two.
+// Requires 2^-100 <= q_scale <= 2^100, which makes every other case one of
+//   |a| < 2^-119 (zero and subnormals included), or a result below 2^-126
+//                                                    -> +-0   (E4M3 +-0),
+//   infinite a, or a result of 2^128 or more         -> +-inf (E4M3 +-448),
+//   NaN a                                            -> NaN.
 __device__ __forceinline__ float div_by_table(uint32_t a16, const uint32_t* tab) {
   const uint32_t e = (a16 >> 7) & 0xFFu;
-  const uint32_t sign = (a16 & 0x8000u) << 16;
-  const uint32_t t = tab[a16 & 0x7Fu];
-  const int er = static_cast<int>(t >> 23) + static_cast<int>(e) - 134;
-  uint32_t r = t + ((e - 134u) << 23);
-  r = (er <= 0 || e == 0u) ? 0u : r;
-  r = (er >= 255 || e == 0xFFu) ? 0x7F800000u : r;
-  r = (e == 0xFFu && (a16 & 0x7Fu)) ? 0x7FC00000u : r;
-  return __uint_as_float(r | sign);
+  const float t = __uint_as_float(tab[a16 & 0x7Fu]);
+  // 2^(E-134) as a float; only used for E >= 8, where it is a normal float.
+  const float scale = __uint_as_float((e - 7u) << 23);
+  // The product is exact or overflows to inf (E4M3 448) or underflows below
+  // 2^-126 (E4M3 0), matching the exact quotient's code.
+  float x = __fmul_rn(t, scale);
+  x = e < 8u ? 0.f : x;                             // |a| < 2^-119: quotient < 2^-19
+  x = e == 0xFFu ? __uint_as_float(a16 << 16) : x;  // inf / NaN pass through
+  return __uint_as_float(__float_as_uint(x) | ((a16 & 0x8000u) << 16));
 }
 
 // Plain IEEE division for q_scale outside the table's range (kept out of
@@ -294,10 +300,16 @@ static __device__ __noinline__ uint32_t e4m3_pair_divide(uint32_t two_bf16, floa
 }
 
 // Two BF16 values (packed) -> two E4M3 codes (packed, low value in byte 0)
-// of value / q_scale: IEEE division, then saturating RNE conversion.
-__device__ __forceinline__ uint32_t e4m3_pair(uint32_t two_bf16, const uint32_t* tab, float qs, bool table_ok) {
-  if (!table_ok) return e4m3_pair_divide(two_bf16, qs);
-  return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
+// of value / q_scale: IEEE division, then saturating RNE conversion.  The
+// table form has no call and no branch, so the conversions of a thread's
+// values interleave freely; the division form is the out-of-range path.
+template <bool TABLE>
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t two_bf16, const uint32_t* tab, float qs) {
+  if constexpr (TABLE) {
+    return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
+  } else {
+    return e4m3_pair_divide(two_bf16, qs);
+  }
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..15) of token row `m` in the
@@ -311,6 +323,62 @@ __device__ __forceinline__ uint32_t q_off(int m, int chunk) {
 // rows stored with the TMA 128B swizzle (chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Step 7 of the kernel: D rows g / g+8 of warp w's MMA tile are latent
+// columns n_cta+16w+g / +8, its columns 2t, 2t+1 are tokens.  After
+// movmatrix.trans a lane holds token 8jt+g and columns 16w+2t, +1 (first
+// block) and 16w+8+2t, +1 (second block); stores go straight to
+// out[m*row_stride + h*576 + n].
+template <int OD, int MT, bool TABLE>
+__device__ __forceinline__ void write_projection(const RunParams& p, const float (&acc)[MT][4], int warp, int lane,
+                                                 int h, int n_cta, const uint32_t* divtab, float qs) {
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  // Phase 1: every value this thread writes, into registers; phase 2: the
+  // stores.  All table reads precede all stores.
+  uint32_t r[MT][2];
+#pragma unroll
+  for (int jt = 0; jt < MT; ++jt) {
+    r[jt][0] = movmatrix_trans(pack_bf16x2(acc[jt][1], acc[jt][0]));
+    r[jt][1] = movmatrix_trans(pack_bf16x2(acc[jt][3], acc[jt][2]));
+  }
+  if constexpr (OD == kOutE4M3) {
+#pragma unroll
+    for (int jt = 0; jt < MT; ++jt) {
+      r[jt][0] = e4m3_pair<TABLE>(r[jt][0], divtab, qs);
+      r[jt][1] = e4m3_pair<TABLE>(r[jt][1], divtab, qs);
+    }
+  }
+#pragma unroll
+  for (int jt = 0; jt < MT; ++jt) {
+    const int m = 8 * jt + g;
+    if (m < p.M) {
+      const size_t off =
+          static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + n_cta + 16 * warp + 2 * t;
+      if constexpr (OD == kOutBF16) {
+        uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + off;
+        *reinterpret_cast<uint32_t*>(o) = r[jt][0];
+        *reinterpret_cast<uint32_t*>(o + 8) = r[jt][1];
+      } else {
+        uint8_t* o = p.out + off;
+        *reinterpret_cast<uint16_t*>(o) = static_cast<uint16_t>(r[jt][0]);
+        *reinterpret_cast<uint16_t*>(o + 8) = static_cast<uint16_t>(r[jt][1]);
+      }
+    }
+  }
+}
+
+// Step 8: the q_pe append for one pair of values (2 BF16 in, 2 BF16 or
+// 2 E4M3 out) at element offset `off` of the output.
+template <int OD, bool TABLE>
+__device__ __forceinline__ void write_pe_pair(const RunParams& p, size_t off, uint32_t pe2, const uint32_t* divtab,
+                                              float qs) {
+  if constexpr (OD == kOutBF16) {
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + off) = pe2;
+  } else {
+    *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<TABLE>(pe2, divtab, qs));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -333,14 +401,17 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int g = lane >> 2;
-  const int t = lane & 3;
   const int H = p.H;
   const int M = p.M;
   const int n_cta = tile * kNTile;
 
   // The next kernel on the stream may start its independent prologue.
   if constexpr (TRIG == 0) pdl_launch_dependents();
+
+  // q_scale is, like the weights, a per-tensor constant of the layer: it is
+  // read (and its division table built) ahead of the dependency wait.
+  float qs = 1.f;
+  if constexpr (OD == kOutE4M3) qs = *p.q_scale;
 
   // 1. Weight (and scale) stream: one elected thread, one barrier phase.
   if (tid == 0) {
@@ -381,26 +452,36 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
     const uint8_t* sc = smem + kSmemScale;
     const int c = tid & 7;
     const int blk = (n_cta + 8 * c) / kMxBlock;
+    // Loads of all 8 jobs first, then the arithmetic, then the stores: the
+    // phases keep every job's chain independent of the others' stores.
+    uint2 v[8];
+    uint32_t xs[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int k = (tid >> 3) + 16 * i;
-      const uint2 v = *reinterpret_cast<const uint2*>(raw + k * kNTile + 8 * c);
-      const uint32_t x = sc[k * (kLatent / kMxBlock) + blk];
-      // value = code * 2^(x-127) = (code * 2^-120) * 2^(x-7), split in two
-      // exact power-of-two factors when 2^(x-7) exceeds BF16's range.
+      v[i] = *reinterpret_cast<const uint2*>(raw + k * kNTile + 8 * c);
+      xs[i] = sc[k * (kLatent / kMxBlock) + blk];
+    }
+    uint32_t o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // value = code * 2^(x-127) = (code * 2^-120) * 2^(x-7), as two exact
+      // power-of-two factors so that each stays inside BF16's range.
+      const uint32_t x = xs[i];
       const uint32_t s1 = pow2_bf16(min(x, 134u));
       const uint32_t f1 = s1 | (s1 << 16);
-      uint32_t o[4];
-      const uint32_t w[2] = {v.x, v.y};
+      // 2^(x-134) for x > 134 (1.0 otherwise); NaN for the NaN byte 255.
+      const uint32_t s2 = x == 255u ? 0x7FC0u : pow2_bf16(max(x, 134u) - 127u);
+      const uint32_t f2 = s2 | (s2 << 16);
+      const uint32_t w[2] = {v[i].x, v[i].y};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) o[q] = mul_bf16x2(e4m3x2_to_bf16x2_scaled(w[q >> 1] >> (16 * (q & 1))), f1);
-      if (x > 134u) {
-        const uint32_t s2 = x == 255u ? 0x7FC0u : pow2_bf16(x - 127u);  // 2^(x-134)
-        const uint32_t f2 = s2 | (s2 << 16);
+      for (int q = 0; q < 4; ++q)
+        o[i][q] = mul_bf16x2(mul_bf16x2(e4m3x2_to_bf16x2_scaled(w[q >> 1] >> (16 * (q & 1))), f1), f2);
+    }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) o[q] = mul_bf16x2(o[q], f2);
-      }
-      *reinterpret_cast<uint4*>(smem + kSmemA + sw128(k, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int i = 0; i < 8; ++i) {
+      const int k = (tid >> 3) + 16 * i;
+      *reinterpret_cast<uint4*>(smem + kSmemA + sw128(k, c)) = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
     }
     __syncthreads();
     if constexpr (TRIG == 2) pdl_launch_dependents();
@@ -413,20 +494,28 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
     pdl_launch_dependents();
   }
 
-  // 4. Wait for the producer of q_nope / q_pe / q_scale (no-op without PDL).
+  // E4M3 output: table of RN((128+f)/q_scale), one entry per thread, made
+  // visible by the barrier after the q_nope tile is stored.
+  uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + kSmemDiv);
+  bool table_ok = false;
+  if constexpr (OD == kOutE4M3) {
+    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
+    if (table_ok) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+  }
+
+  // 4. Wait for the producer of q_nope / q_pe (no-op without PDL).
   pdl_wait();
   if constexpr (TRIG == 1) pdl_launch_dependents();
 
-  // 5. Inputs: this head's q_nope rows [8*MT][128] (16-byte loads, rows >= M
-  //    zero), this thread's q_pe chunk (if any) and q_scale, all issued back
-  //    to back; then the weight fragments, which need no input.
-  // q_pe chunk (8 elements) of this thread: the head's M*8 chunks are dealt
-  // round-robin to its 8 CTAs and, inside a CTA, to every 4th thread, so
-  // every CTA and warp gets an equal share (at most one chunk per thread).
-  const int nchunks_pe = M * (kRope / 8);
-  const int c_pe = (tid & 3) == 0 ? tile + kTilesPerHead * (tid >> 2) : nchunks_pe;
-  uint4 pe = make_uint4(0u, 0u, 0u, 0u);
-  if (c_pe < nchunks_pe) pe = ld_u128(p.q_pe + (static_cast<size_t>(c_pe >> 3) * H + h) * kRope + 8 * (c_pe & 7));
+  // 5. Inputs: this thread's q_pe pair and this head's q_nope rows
+  //    [8*MT][128] (16-byte loads, rows >= M zero), issued back to back; then
+  //    the weight fragments, which need no input.  q_pe pair j (values 2j,
+  //    2j+1 of the head's M x 64 q_pe block) belongs to thread j - 128*tile.
+  const int j_pe = tile * kThreads + tid;
+  const bool has_pe = j_pe < M * (kRope / 2);
+  const int m_pe = j_pe >> 5;
+  uint32_t pe = 0u;
+  if (has_pe) pe = ld_u32(p.q_pe + (static_cast<size_t>(m_pe) * H + h) * kRope + 2 * (j_pe & 31));
   uint4 qv[MT];
 #pragma unroll
   for (int i = 0; i < MT; ++i) {
@@ -435,8 +524,6 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
     qv[i] = make_uint4(0u, 0u, 0u, 0u);
     if (m < M) qv[i] = ld_u128(p.q_nope + (static_cast<size_t>(m) * H + h) * kNope + 8 * (c & 15));
   }
-  float qs = 1.f;
-  if constexpr (OD == kOutE4M3) qs = *p.q_scale;
 
   if constexpr (WF == kWeightBF16 && TRIG != 2) {
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
@@ -454,19 +541,23 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
 #pragma unroll
   for (int s = 0; s < 8; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
 
-  // E4M3 output: table of RN((128+f)/q_scale), one entry per thread.
-  uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + kSmemDiv);
-  bool table_ok = false;
-  if constexpr (OD == kOutE4M3) {
-    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
-    if (table_ok) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
-  }
 #pragma unroll
   for (int i = 0; i < MT; ++i) {
     const int c = tid + kThreads * i;
     *reinterpret_cast<uint4*>(smem + kSmemQ + q_off(c >> 4, c & 15)) = qv[i];
   }
   __syncthreads();
+
+  // 8. (ahead of the contraction, overlapping its latency) the q_pe append.
+  if (has_pe) {
+    const size_t off = static_cast<size_t>(m_pe) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + kLatent +
+                       2 * (j_pe & 31);
+    if (OD == kOutBF16 || table_ok) {
+      write_pe_pair<OD, true>(p, off, pe, divtab, qs);
+    } else {
+      write_pe_pair<OD, false>(p, off, pe, divtab, qs);
+    }
+  }
 
   // 6. Contraction, two independent accumulator chains (even / odd k-steps).
   //    B (q_nope): matrix L>>3 of ldmatrix is k chunk 2s2*2 + (L>>3) of tokens
@@ -492,46 +583,14 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[0][jt][e] += acc[1][jt][e];
 
-  // 7. Epilogue.  D rows g / g+8 are columns n_cta+16w+g / +8, columns 2t,
-  //    2t+1 are tokens.  After movmatrix.trans a lane holds token 8jt+g and
-  //    columns 16w+2t, +1 (first block) and 16w+8+2t, +1 (second block).
-#pragma unroll
-  for (int jt = 0; jt < MT; ++jt) {
-    const uint32_t r0 = movmatrix_trans(pack_bf16x2(acc[0][jt][1], acc[0][jt][0]));
-    const uint32_t r1 = movmatrix_trans(pack_bf16x2(acc[0][jt][3], acc[0][jt][2]));
-    const int m = 8 * jt + g;
-    if (m < M) {
-      const size_t off =
-          static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + n_cta + 16 * warp + 2 * t;
-      if constexpr (OD == kOutBF16) {
-        uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + off;
-        *reinterpret_cast<uint32_t*>(o) = r0;
-        *reinterpret_cast<uint32_t*>(o + 8) = r1;
-      } else {
-        uint8_t* o = p.out + off;
-        *reinterpret_cast<uint16_t*>(o) = static_cast<uint16_t>(e4m3_pair(r0, divtab, qs, table_ok));
-        *reinterpret_cast<uint16_t*>(o + 8) = static_cast<uint16_t>(e4m3_pair(r1, divtab, qs, table_ok));
-      }
-    }
-  }
-
-  // 8. Append q_pe (chunk loaded right after the dependency wait).
-  if (c_pe < nchunks_pe) {
-    const int m = c_pe >> 3;
-    const int part = c_pe & 7;
-    const size_t off =
-        static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + kLatent + 8 * part;
-    if constexpr (OD == kOutBF16) {
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + off) = pe;
-    } else {
-      const uint32_t in[4] = {pe.x, pe.y, pe.z, pe.w};
-      uint32_t w[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        w[i] = e4m3_pair(in[2 * i], divtab, qs, table_ok) | (e4m3_pair(in[2 * i + 1], divtab, qs, table_ok) << 16);
-      }
-      *reinterpret_cast<uint2*>(p.out + off) = make_uint2(w[0], w[1]);
-    }
+  // 7. Epilogue; the E4M3 division form is chosen once per CTA so that the
+  //    common path holds no call and no branch.
+  if constexpr (OD == kOutBF16) {
+    write_projection<OD, MT, true>(p, acc[0], warp, lane, h, n_cta, divtab, qs);
+  } else if (table_ok) {
+    write_projection<OD, MT, true>(p, acc[0], warp, lane, h, n_cta, divtab, qs);
+  } else {
+    write_projection<OD, MT, false>(p, acc[0], warp, lane, h, n_cta, divtab, qs);
   }
 }
 
