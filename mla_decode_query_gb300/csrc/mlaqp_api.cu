@@ -39,8 +39,16 @@ int fail_cuda(const char* what, cudaError_t e) {
 bool supported_heads(int h) { return h == 8 || h == 11 || h == 16; }
 
 constexpr int kMaxDevices = 64;
-// 0 = not yet queried, 1 = sm_103, 2 = another architecture.
-std::atomic<int> g_device_state[kMaxDevices];
+
+// Per-device facts the launch policy needs, queried once.
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 = not yet queried, 1 = sm_103 and set up, 2 = another architecture
+  int smem_per_sm = 0;        // bytes of shared memory per SM
+  int reserved_per_block = 0; // bytes the driver reserves per resident CTA
+  int max_smem_optin = 0;     // largest dynamic shared memory a CTA may request
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
 // Bit (wf*2+od)*4 + (mt-1) set once that specialisation's image is loaded.
 std::atomic<uint32_t> g_prewarmed[kMaxDevices];
 std::mutex g_prewarm_mutex;
@@ -55,16 +63,41 @@ int resolve_device(int device, int* out) {
   return MLAQP_OK;
 }
 
-// MLAQP_OK if `device` is an sm_103 GPU, else an error status + message.
+// Largest dynamic shared memory any launch policy below requests.
+int policy_max_smem(const DeviceInfo& d);
+// Raises every kernel's dynamic-shared-memory limit to what the launch
+// policy may request on this device (current device must be `device`).
+int setup_kernels(const DeviceInfo& d);
+
+// MLAQP_OK if `device` is an sm_103 GPU (and its kernels are set up), else
+// an error status + message.  The first call per device queries it and
+// sets kernel attributes; it synchronises nothing and launches nothing.
 int check_device(int device) {
-  int state = g_device_state[device].load(std::memory_order_acquire);
+  DeviceInfo& d = g_dev[device];
+  int state = d.state.load(std::memory_order_acquire);
   if (state == 0) {
-    int major = 0, minor = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
-    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute", e);
-    state = (major == 10 && minor == 3) ? 1 : 2;
-    g_device_state[device].store(state, std::memory_order_release);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    state = d.state.load(std::memory_order_acquire);
+    if (state == 0) {
+      int major = 0, minor = 0;
+      cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.reserved_per_block, cudaDevAttrReservedSharedMemoryPerBlock, device);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+      if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute", e);
+      state = (major == 10 && minor == 3) ? 1 : 2;
+      if (state == 1) {
+        int prev = -1;
+        e = cudaGetDevice(&prev);
+        if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+        if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess) return fail_cuda("cudaSetDevice", e);
+        const int st = setup_kernels(d);
+        if (prev != device) cudaSetDevice(prev);
+        if (st != MLAQP_OK) return st;
+      }
+      d.state.store(state, std::memory_order_release);
+    }
   }
   if (state != 1) return fail(MLAQP_ERR_UNSUPPORTED, "device is not an sm_103 (GB300) GPU");
   return MLAQP_OK;
@@ -116,17 +149,39 @@ int encode_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
   return MLAQP_OK;
 }
 
-// Where a PDL-launched CTA lets the next kernel start (see the kernel),
-// chosen from per-layer times of 128-layer CUDA-graph chains on GB300:
-// BF16 weights stream fast enough that triggering after the dependency wait
-// (two kernels in flight, CTAs spread over distinct SMs) wins at every M;
-// MXFP8 tiles need their copy and dequantisation ahead of the wait, so M <= 8
-// triggers at entry (deep overlap); larger M, whose heavier epilogue suffers
-// when CTAs of early-launched kernels share SMs, triggers after the wait.
-int trigger_policy(int weight_format, int mt) {
-  if (weight_format == MLAQP_WEIGHT_BF16) return 1;
-  return mt == 1 ? 0 : 1;
+// Launch policy of one call: where a PDL-launched CTA lets the next kernel
+// start (see the kernel) and an optional cap on resident CTAs per SM,
+// imposed by padding the dynamic shared memory.  Chosen from per-layer times
+// of 128-layer CUDA-graph chains on GB300:
+//   * BF16 weights, M <= 8: trigger at entry, at most 3 CTAs per SM -- the
+//     weight stream overlaps the previous layers while early-launched
+//     kernels cannot crowd many of their CTAs onto a few SMs;
+//   * BF16 weights, M > 8: trigger after the dependency wait (two kernels in
+//     flight, one CTA per SM), since the heavier epilogue suffers most when
+//     CTAs share an SM;
+//   * MXFP8 weights need their copy and dequantisation ahead of the wait:
+//     entry trigger, uncapped for M <= 4 and capped at 3 CTAs per SM up to
+//     M = 16; after the wait for M > 16.
+struct LaunchPolicy {
+  int trig;     // 0 entry, 1 after the wait, 2 weights ready
+  int cta_cap;  // 0: none, else resident CTAs per SM
+};
+
+LaunchPolicy launch_policy(int weight_format, int M) {
+  if (weight_format == MLAQP_WEIGHT_BF16) return M <= 8 ? LaunchPolicy{0, 3} : LaunchPolicy{1, 0};
+  if (M <= 4) return LaunchPolicy{0, 0};
+  return M <= 16 ? LaunchPolicy{0, 3} : LaunchPolicy{1, 0};
 }
+
+// Dynamic shared memory that realises `cap` CTAs per SM for a kernel that
+// needs `base` bytes.
+int smem_for_cap(const DeviceInfo& d, int base, int cap) {
+  if (cap <= 0) return base;
+  const int bytes = d.smem_per_sm / cap - d.reserved_per_block;
+  return bytes > base ? (bytes < d.max_smem_optin ? bytes : d.max_smem_optin) : base;
+}
+
+int policy_max_smem(const DeviceInfo& d) { return smem_for_cap(d, mlaqp::kSmemBytes, 3); }
 
 const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig) {
   const int mt = (M + 7) / 8;
@@ -136,8 +191,17 @@ const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig) {
   return &table[out_dtype][mt - 1][trig];
 }
 
-const KernelInfo* lookup(int weight_format, int out_dtype, int M) {
-  return lookup(weight_format, out_dtype, M, trigger_policy(weight_format, (M + 7) / 8));
+int setup_kernels(const DeviceInfo& d) {
+  const int smem = policy_max_smem(d);
+  for (int wf = 0; wf < 2; ++wf)
+    for (int od = 0; od < 2; ++od)
+      for (int mt = 1; mt <= 4; ++mt)
+        for (int trig = 0; trig < mlaqp::kTrigVariants; ++trig) {
+          const KernelInfo* k = lookup(wf, od, 8 * mt, trig);
+          const cudaError_t e = cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+          if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+        }
+  return MLAQP_OK;
 }
 
 bool valid_enums(int weight_format, int out_dtype) {
@@ -203,7 +267,9 @@ int run_impl(const void* q_nope, const void* q_pe, const void* weight, const voi
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  const KernelInfo* k = lookup(weight_format, out_dtype, M);
+  const LaunchPolicy pol = launch_policy(weight_format, M);
+  const KernelInfo* k = lookup(weight_format, out_dtype, M, pol.trig);
+  const int smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   RunParams params;
   st = encode_weight_map(&params.wmap, weight, H, mx);
   if (st != MLAQP_OK) return st;
@@ -221,7 +287,7 @@ int run_impl(const void* q_nope, const void* q_pe, const void* weight, const voi
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H), 1);
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(k->smem_bytes);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   if (pdl) {
@@ -306,7 +372,7 @@ int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight, cons
 int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas, int* threads_per_cta) {
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
-  const KernelInfo* k = lookup(weight_format, out_dtype, M);
+  const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, M).trig);
   if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
   if (threads_per_cta) *threads_per_cta = k->threads;
   return MLAQP_OK;
