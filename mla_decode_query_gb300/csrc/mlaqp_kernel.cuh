@@ -55,7 +55,12 @@ constexpr int kMaxM = 32;
 
 constexpr int kNTile = 64;                       // latent columns per CTA
 constexpr int kWarps = kNTile / 16;              // one 16-column MMA tile per warp
-constexpr int kThreads = kWarps * 32;            // 128
+constexpr int kThreads = kWarps * 32;            // 128 threads per token group
+
+// Token groups per CTA: for M > 8 (two or more 8-token MMA column tiles) a
+// second group of four warps takes every other token tile, halving each
+// warp's MMA and epilogue work; M <= 8 uses one group.
+constexpr int token_groups(int mt) { return mt >= 2 ? 2 : 1; }
 constexpr int kTilesPerHead = kLatent / kNTile;  // 8
 
 // Dynamic shared memory layout (offsets from a 1024-byte aligned base).
@@ -330,9 +335,10 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // movmatrix.trans a lane holds token 8jt+g and columns 16w+2t, +1 (first
 // block) and 16w+8+2t, +1 (second block); stores go straight to
 // out[m*row_stride + h*576 + n].
-template <int OD, int MT, bool TABLE>
-__device__ __forceinline__ void write_projection(const RunParams& p, const float (&acc)[MT][4], int warp, int lane,
-                                                 int h, int n_cta, const uint32_t* divtab, float qs) {
+template <int OD, int MTW, int TS, bool TABLE>
+__device__ __forceinline__ void write_projection(const RunParams& p, const float (&acc)[MTW][4], int wcol, int wtok,
+                                                 int lane, int h, int n_cta, const uint32_t* divtab, float qs) {
+  constexpr int MT = MTW;  // this warp's token tiles: jt = wtok + TS*i, i < MTW
   const int g = lane >> 2;
   const int t = lane & 3;
   // Phase 1: every value this thread writes, into registers; phase 2: the
@@ -352,10 +358,10 @@ __device__ __forceinline__ void write_projection(const RunParams& p, const float
   }
 #pragma unroll
   for (int jt = 0; jt < MT; ++jt) {
-    const int m = 8 * jt + g;
+    const int m = 8 * (wtok + TS * jt) + g;  // beyond the last tile m >= M: no store
     if (m < p.M) {
       const size_t off =
-          static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + n_cta + 16 * warp + 2 * t;
+          static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + n_cta + 16 * wcol + 2 * t;
       if constexpr (OD == kOutBF16) {
         uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + off;
         *reinterpret_cast<uint32_t*>(o) = r[jt][0];
@@ -389,8 +395,10 @@ __device__ __forceinline__ void write_pe_pair(const RunParams& p, size_t off, ui
 //   2 = once its weight tile is in shared memory (MXFP8: dequantised).
 // ---------------------------------------------------------------------------
 
-template <int WF, int OD, int MT, int TRIG>
-__global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __grid_constant__ RunParams p) {
+template <int WF, int OD, int MT, int TRIG, int TS = token_groups(MT)>
+__global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const __grid_constant__ RunParams p) {
+  constexpr int kCta = kThreads * TS;       // threads in the CTA
+  constexpr int MTW = (MT + TS - 1) / TS;   // token tiles per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_a = smem_u32(smem + kSmemA);
@@ -401,6 +409,8 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int wcol = warp & (kWarps - 1);  // 16-column MMA tile of this warp
+  const int wtok = warp / kWarps;        // token group of this warp
   const int H = p.H;
   const int M = p.M;
   const int n_cta = tile * kNTile;
@@ -441,7 +451,7 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
   __syncthreads();  // barrier initialised before anyone waits on it
 
   // 3. MXFP8: dequantise into the swizzled BF16 tile before the dependency
-  //    wait.  Job (row k, chunk c of 8 columns); 1024 jobs, 8 per thread.
+  //    wait.  Job (row k, chunk c of 8 columns); 1024 jobs, 8/TS per thread.
   if constexpr (WF == kWeightMXFP8) {
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
@@ -452,19 +462,20 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
     const uint8_t* sc = smem + kSmemScale;
     const int c = tid & 7;
     const int blk = (n_cta + 8 * c) / kMxBlock;
-    // Loads of all 8 jobs first, then the arithmetic, then the stores: the
+    // Loads of all jobs first, then the arithmetic, then the stores: the
     // phases keep every job's chain independent of the others' stores.
-    uint2 v[8];
-    uint32_t xs[8];
+    constexpr int kJobs = 8 / TS;
+    uint2 v[kJobs];
+    uint32_t xs[kJobs];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int k = (tid >> 3) + 16 * i;
+    for (int i = 0; i < kJobs; ++i) {
+      const int k = (tid >> 3) + (kCta / 8) * i;
       v[i] = *reinterpret_cast<const uint2*>(raw + k * kNTile + 8 * c);
       xs[i] = sc[k * (kLatent / kMxBlock) + blk];
     }
-    uint32_t o[8][4];
+    uint32_t o[kJobs][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kJobs; ++i) {
       // value = code * 2^(x-127) = (code * 2^-120) * 2^(x-7), as two exact
       // power-of-two factors so that each stays inside BF16's range.
       const uint32_t x = xs[i];
@@ -479,8 +490,8 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
         o[i][q] = mul_bf16x2(mul_bf16x2(e4m3x2_to_bf16x2_scaled(w[q >> 1] >> (16 * (q & 1))), f1), f2);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int k = (tid >> 3) + 16 * i;
+    for (int i = 0; i < kJobs; ++i) {
+      const int k = (tid >> 3) + (kCta / 8) * i;
       *reinterpret_cast<uint4*>(smem + kSmemA + sw128(k, c)) = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
     }
     __syncthreads();
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
   bool table_ok = false;
   if constexpr (OD == kOutE4M3) {
     table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
-    if (table_ok) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+    if (table_ok && tid < 128) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
   }
 
   // 4. Wait for the producer of q_nope / q_pe (no-op without PDL).
@@ -510,19 +521,21 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
   // 5. Inputs: this thread's q_pe pair and this head's q_nope rows
   //    [8*MT][128] (16-byte loads, rows >= M zero), issued back to back; then
   //    the weight fragments, which need no input.  q_pe pair j (values 2j,
-  //    2j+1 of the head's M x 64 q_pe block) belongs to thread j - 128*tile.
-  const int j_pe = tile * kThreads + tid;
+  //    2j+1 of the head's M x 64 q_pe block) belongs to thread j - kCta*tile.
+  const int j_pe = tile * kCta + tid;
   const bool has_pe = j_pe < M * (kRope / 2);
   const int m_pe = j_pe >> 5;
   uint32_t pe = 0u;
   if (has_pe) pe = ld_u32(p.q_pe + (static_cast<size_t>(m_pe) * H + h) * kRope + 2 * (j_pe & 31));
-  uint4 qv[MT];
+  constexpr int kQChunks = 128 * MT;  // 16-byte chunks of the [8*MT][128] tile
+  constexpr int QI = (kQChunks + kCta - 1) / kCta;
+  uint4 qv[QI];
 #pragma unroll
-  for (int i = 0; i < MT; ++i) {
-    const int c = tid + kThreads * i;  // chunk c: token row c/16, k chunk c%16
+  for (int i = 0; i < QI; ++i) {
+    const int c = tid + kCta * i;  // chunk c: token row c/16, k chunk c%16
     const int m = c >> 4;
     qv[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M) qv[i] = ld_u128(p.q_nope + (static_cast<size_t>(m) * H + h) * kNope + 8 * (c & 15));
+    if (c < kQChunks && m < M) qv[i] = ld_u128(p.q_nope + (static_cast<size_t>(m) * H + h) * kNope + 8 * (c & 15));
   }
 
   if constexpr (WF == kWeightBF16 && TRIG != 2) {
@@ -536,15 +549,15 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
   // lane L addresses row L&7 of matrix L>>3 -- matrices 0/1 = k 16s..+7,
   // 2/3 = k 16s+8..+15; 0/2 = columns 16w..+7, 1/3 = 16w+8..+15.
   const int mi = lane >> 3;
-  const int chunk = 2 * warp + (mi & 1);
+  const int chunk = 2 * wcol + (mi & 1);
   uint32_t a[8][4];
 #pragma unroll
   for (int s = 0; s < 8; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
 
 #pragma unroll
-  for (int i = 0; i < MT; ++i) {
-    const int c = tid + kThreads * i;
-    *reinterpret_cast<uint4*>(smem + kSmemQ + q_off(c >> 4, c & 15)) = qv[i];
+  for (int i = 0; i < QI; ++i) {
+    const int c = tid + kCta * i;
+    if (c < kQChunks) *reinterpret_cast<uint4*>(smem + kSmemQ + q_off(c >> 4, c & 15)) = qv[i];
   }
   __syncthreads();
 
@@ -559,38 +572,43 @@ __global__ void __launch_bounds__(kThreads) mlaqp_fused_query_kernel(const __gri
     }
   }
 
-  // 6. Contraction, two independent accumulator chains (even / odd k-steps).
-  //    B (q_nope): matrix L>>3 of ldmatrix is k chunk 2s2*2 + (L>>3) of tokens
-  //    8jt..8jt+7, giving b0/b1 of steps 2*s2 and 2*s2+1.
+  // 6. Contraction, two independent accumulator chains (even / odd k-steps),
+  //    over this warp's token tiles jt = wtok + TS*i.  B (q_nope): matrix L>>3
+  //    of ldmatrix is k chunk 4*s2 + (L>>3) of tokens 8jt..8jt+7, giving
+  //    b0/b1 of steps 2*s2 and 2*s2+1.
   const uint32_t s_q = smem_u32(smem + kSmemQ);
-  uint32_t b[4][MT][4];
+  bool tile_ok[MTW];
+#pragma unroll
+  for (int i = 0; i < MTW; ++i) tile_ok[i] = wtok + TS * i < MT;  // uniform per warp
+  uint32_t b[4][MTW][4];
 #pragma unroll
   for (int s2 = 0; s2 < 4; ++s2)
 #pragma unroll
-    for (int jt = 0; jt < MT; ++jt) ldmatrix_x4(b[s2][jt], s_q + q_off(8 * jt + (lane & 7), 4 * s2 + mi));
-  float acc[2][MT][4];
+    for (int i = 0; i < MTW; ++i)
+      if (tile_ok[i]) ldmatrix_x4(b[s2][i], s_q + q_off(8 * (wtok + TS * i) + (lane & 7), 4 * s2 + mi));
+  float acc[2][MTW][4];
 #pragma unroll
   for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-    for (int jt = 0; jt < MT; ++jt) acc[c2][jt][0] = acc[c2][jt][1] = acc[c2][jt][2] = acc[c2][jt][3] = 0.f;
+    for (int i = 0; i < MTW; ++i) acc[c2][i][0] = acc[c2][i][1] = acc[c2][i][2] = acc[c2][i][3] = 0.f;
 #pragma unroll
   for (int s = 0; s < 8; ++s)
 #pragma unroll
-    for (int jt = 0; jt < MT; ++jt)
-      mma_bf16_16816(acc[s & 1][jt], a[s], b[s >> 1][jt][2 * (s & 1)], b[s >> 1][jt][2 * (s & 1) + 1]);
+    for (int i = 0; i < MTW; ++i)
+      if (tile_ok[i]) mma_bf16_16816(acc[s & 1][i], a[s], b[s >> 1][i][2 * (s & 1)], b[s >> 1][i][2 * (s & 1) + 1]);
 #pragma unroll
-  for (int jt = 0; jt < MT; ++jt)
+  for (int i = 0; i < MTW; ++i)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[0][jt][e] += acc[1][jt][e];
+    for (int e = 0; e < 4; ++e) acc[0][i][e] += acc[1][i][e];
 
   // 7. Epilogue; the E4M3 division form is chosen once per CTA so that the
   //    common path holds no call and no branch.
   if constexpr (OD == kOutBF16) {
-    write_projection<OD, MT, true>(p, acc[0], warp, lane, h, n_cta, divtab, qs);
+    write_projection<OD, MTW, TS, true>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs);
   } else if (table_ok) {
-    write_projection<OD, MT, true>(p, acc[0], warp, lane, h, n_cta, divtab, qs);
+    write_projection<OD, MTW, TS, true>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs);
   } else {
-    write_projection<OD, MT, false>(p, acc[0], warp, lane, h, n_cta, divtab, qs);
+    write_projection<OD, MTW, TS, false>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs);
   }
 }
 

@@ -8,7 +8,7 @@ constexpr int kWF = kWeightMXFP8;
 
 template <int OD, int MT, int TRIG>
 KernelInfo entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT, TRIG>), kThreads,
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT, TRIG>), kThreads * token_groups(MT),
                     kTilesPerHead, kSmemBytes};
 }
 

@@ -99,9 +99,10 @@ def test_can_implement_domain(built_library):
 
 def test_launch_shape(built_library):
     for h in (8, 11, 16):
-        for m in (1, 9, 32):
+        for m in (1, 8, 9, 32):
             st, grid, threads = mq.mlaqp_launch_shape(m, h, "mxfp8", "e4m3")
-            assert st == mq.MLAQP_OK and grid == 8 * h and threads == 128
+            # one 4-warp token group up to M=8, two groups above
+            assert st == mq.MLAQP_OK and grid == 8 * h and threads == (128 if m <= 8 else 256)
     assert mq.mlaqp_launch_shape(0, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(4, 12)[0] == mq.MLAQP_ERR_UNSUPPORTED
 
