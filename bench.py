@@ -352,10 +352,19 @@ def run_gpu(args):
     launches = args.steps * sum(s.L for s, _ in points)
     dominant = max(kern_ms, key=kern_ms.get)
     ach = kern_bytes[dominant] / (kern_ms[dominant] * 1e-3) / 1e9
+    traffic_table = measured_traffic()
+    traffic = None
+    dom_points = [(s, M) for s, M in points if f"{s.weight_format}->{s.out_dtype}" == dominant]
+    if traffic_table and all((dominant, M) in traffic_table for _, M in dom_points):
+        traffic = round(sum(traffic_table[(dominant, M)] * s.L for s, M in dom_points) /
+                        sum(s.L for s, _ in dom_points))
     roof = {"bound": "hbm", "kernel": f"mlaqp_fused_query_kernel ({dominant})",
             "achieved": round(ach, 1), "peak": peaks[0], "unit": "GB/s",
-            "frac": round(ach / peaks[0], 4), "peak_source": peaks[1], "traffic": None,
+            "frac": round(ach / peaks[0], 4), "peak_source": peaks[1], "traffic": traffic,
+            "traffic_source": TRAFFIC_FILE if traffic else "kernel changed since the last ncu capture",
+            "algorithmic_bytes_per_launch": round(kern_bytes[dominant] / (args.steps * sum(s.L for s, _ in dom_points))),
             "per_kernel_gbs": {f: round(kern_bytes[f] / (kern_ms[f] * 1e-3) / 1e9, 1) for f in kern_ms}}
+    floor = launch_floor(args.steps, args.warmup)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
@@ -367,6 +376,7 @@ def run_gpu(args):
                              f"vs L2 {L2_BYTES >> 20} MiB (inputs larger than L2, no flush)",
                        "parallelism": f"replicas{ws}"},
             "us_per_layer_mean": round(1e3 * total_ms / args.steps / sum(s.L for s, _ in points), 4),
+            "launch_floor_us": floor,
             "points": per_point,
             "roofline": roof,
             "gpu_launches": launches,
@@ -415,6 +425,69 @@ def run_e2e(sets, graphs, points, args):
     nbytes = sum(s.bytes_per_call(M) * s.L for s, M in points) * args.steps
     return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms / args.steps, 4)}
+
+
+KERNEL_SOURCES = ("mla_decode_query_gb300/csrc/mlaqp_kernel.cuh", "mla_decode_query_gb300/csrc/mlaqp_kernels_bf16.cu",
+                  "mla_decode_query_gb300/csrc/mlaqp_kernels_mxfp8.cu")
+TRAFFIC_FILE = "profiles/fused_query_dram_traffic_h16.txt"
+
+
+def kernel_source_hash():
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """Per-(pair, M) DRAM bytes per launch from the committed ncu summary, or
+    None when the kernel sources changed since those counters were taken."""
+    root = os.path.dirname(os.path.abspath(__file__))
+    try:
+        lines = open(os.path.join(root, TRAFFIC_FILE)).read().splitlines()
+    except OSError:
+        return None
+    tag = [l for l in lines if l.startswith("# kernel-source-sha256-16")]
+    if not tag or tag[0].split()[2] != kernel_source_hash():
+        return None
+    out = {}
+    for l in lines:
+        if l and not l.startswith("#"):
+            pair, M, traffic, _ = l.split()
+            out[(pair, int(M))] = int(traffic)
+    return out
+
+
+def launch_floor(steps, warmup):
+    """us per launch of a CUDA graph of 128 dependent empty kernels (128 CTAs
+    x 128 threads) with and without programmatic dependent launch: the floor
+    of any one-launch-per-layer chain on this GPU."""
+    import torch
+    import mla_decode_query_gb300 as mq
+    res = {}
+    for pdl in (True, False):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            mq.check(mq.mlaqp_debug_launch_null(128, 128, pdl, stream=s))
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(128):
+                mq.check(mq.mlaqp_debug_launch_null(128, 128, pdl))
+        for _ in range(max(3, warmup)):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(max(5, steps)):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        res["pdl" if pdl else "no_pdl"] = round(1e3 * a.elapsed_time(b) / max(5, steps) / 128, 4)
+    return res
 
 
 def load_peaks():

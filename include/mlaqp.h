@@ -172,6 +172,17 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
                                  int out_dtype, unsigned long long wait_limit_ns,
                                  unsigned int extra_tx_bytes, mlaqp_stream_t stream);
 
+/*
+ * Diagnostic (no counterpart on the pages): launches a kernel of `ctas` x
+ * `threads` that does nothing but the programmatic-launch protocol (trigger
+ * the next kernel, wait for the previous one), with (pdl != 0) or without
+ * programmatic dependent launch.  A CUDA graph of such launches measures the
+ * per-launch floor of a dependent chain, the bound on any one-launch-per-
+ * layer operation.  Returns MLAQP_OK, MLAQP_ERR_INVALID_ARG or
+ * MLAQP_ERR_CUDA.
+ */
+int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t stream);
+
 /* Message of the last non-OK status returned on this thread ("" if none). */
 const char* mlaqp_last_error(void);
 

@@ -23,6 +23,7 @@ from .mlaqp import (  # noqa: F401
     header_functions,
     load_library,
     mlaqp_can_implement,
+    mlaqp_debug_launch_null,
     mlaqp_debug_run_bounded_wait,
     mlaqp_device_status,
     mlaqp_last_error,

@@ -22,6 +22,14 @@
 
 namespace {
 
+// Diagnostic: a kernel with no work but the programmatic-launch protocol
+// (trigger, dependency wait), to measure the floor a chain of dependent
+// launches costs on this GPU.
+__global__ void mlaqp_null_kernel() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 using mlaqp::KernelInfo;
 using mlaqp::RunParams;
 
@@ -395,6 +403,26 @@ int mlaqp_device_status(unsigned int* status, int reset) {
   if (e == cudaSuccess) e = mlaqp::device_status_mxfp8_weights(&b, reset != 0);
   if (e != cudaSuccess) return fail_cuda("reading the device status word", e);
   *status = a | b;
+  return MLAQP_OK;
+}
+
+int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t stream) {
+  if (ctas < 1 || ctas > 65535 || threads < 1 || threads > 1024)
+    return fail(MLAQP_ERR_INVALID_ARG, "ctas must be in 1..65535 and threads in 1..1024");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {nullptr};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&mlaqp_null_kernel), args);
+  if (e != cudaSuccess) return fail_cuda("cudaLaunchKernelExC", e);
   return MLAQP_OK;
 }
 

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "mlaqp_debug_run_bounded_wait": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                               ctypes.c_int64, _c_void_p, _c_int, _c_int, _c_int, _c_int,
                                               ctypes.c_ulonglong, ctypes.c_uint, _c_void_p]),
+    "mlaqp_debug_launch_null": (_c_int, [_c_int, _c_int, _c_int, _c_void_p]),
     "mlaqp_last_error": (ctypes.c_char_p, []),
     "mlaqp_version": (_c_int, []),
 }
@@ -156,6 +157,10 @@ def mlaqp_debug_run_bounded_wait(q_nope, q_pe, weight, weight_scale, out, out_ro
                   out_dtype)
     return load_library().mlaqp_debug_run_bounded_wait(*a, int(wait_limit_ns), int(extra_tx_bytes),
                                                        _stream(stream))
+
+
+def mlaqp_debug_launch_null(ctas, threads, pdl, stream=None) -> int:
+    return load_library().mlaqp_debug_launch_null(int(ctas), int(threads), 1 if pdl else 0, _stream(stream))
 
 
 def mlaqp_launch_shape(M, H, weight_format="bf16", out_dtype="bf16"):
