@@ -21,8 +21,9 @@
  *     library never allocates, frees or synchronises on the run path.
  *   - Supported domain (vLLM PR #174, section What: "capability-gated"
  *     H = 8/11/16 and M = 1..32): num_heads H in {8, 11, 16}, tokens
- *     1 <= M <= 32, nope dim 128, latent dim 512, rope dim 64, on an
- *     sm_103 (GB300) device.
+ *     1 <= M <= 32, nope dim 128 (192, the GLM dim of SparkInfer PR #75,
+ *     section What, through mlaqp_run_strided), latent dim 512, rope dim 64,
+ *     on an sm_103 (GB300) device.
  *   - Status codes are the mlaqp_status values; on any non-OK status a
  *     message is available from mlaqp_last_error() on the same thread.
  *
@@ -115,9 +116,9 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
  *                  out_row_stride * element size a multiple of 16 bytes
  *   M              0 returns MLAQP_OK without launching; 1..32 supported
  *
- * Every pointer must be 16-byte aligned (q_scale: 4-byte aligned); the
- * bytes written to `out` may not overlap any input.  Errors are reported
- * before anything is launched.
+ * q_nope, weight, weight_scale and out must be 16-byte aligned, q_pe and
+ * q_scale 4-byte aligned; the bytes written to `out` may not overlap any
+ * input.  Errors are reported before anything is launched.
  */
 int mlaqp_run(const void* q_nope, const void* q_pe, const void* weight,
               const void* weight_scale, void* out, int64_t out_row_stride,
@@ -139,6 +140,25 @@ int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
                   const void* weight_scale, void* out, int64_t out_row_stride,
                   const float* q_scale, int M, int H, int weight_format, int out_dtype,
                   mlaqp_stream_t stream);
+
+/*
+ * General form of mlaqp_run / mlaqp_run_pdl (pdl != 0): the same operation
+ * with nope dim `nope_dim` (128 or 192) and strided inputs, so that q_nope
+ * and q_pe can be views into the upstream per-head [.., nope_dim + 64]
+ * projection output, or head-major [H, M, nope_dim] (the layout of the
+ * SparkInfer PR #75 BMM, section What), without a copy:
+ *   q_nope element (m,h,k) at q_nope[m*q_nope_token_stride + h*q_nope_head_stride + k]
+ *   q_pe   element (m,h,j) at q_pe[m*q_pe_token_stride + h*q_pe_head_stride + j]
+ * Strides are in elements, >= 0; q_nope strides must be multiples of 8
+ * (16-byte rows), q_pe strides multiples of 2.  weight is [H, nope_dim, 512]
+ * (BF16 or E4M3) and weight_scale [H, nope_dim, 16]; everything else is as
+ * for mlaqp_run.
+ */
+int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride,
+                      const void* q_pe, int64_t q_pe_token_stride, int64_t q_pe_head_stride,
+                      const void* weight, const void* weight_scale, void* out,
+                      int64_t out_row_stride, const float* q_scale, int M, int H, int nope_dim,
+                      int weight_format, int out_dtype, int pdl, mlaqp_stream_t stream);
 
 /*
  * Launch geometry a run with these arguments uses (for reporting): grid size

@@ -31,6 +31,7 @@ from .mlaqp import (  # noqa: F401
     mlaqp_prewarm,
     mlaqp_run,
     mlaqp_run_pdl,
+    mlaqp_run_strided,
     mlaqp_version,
 )
 

@@ -138,16 +138,16 @@ EncodeTiledFn encode_tiled_fn(std::string* err) {
   return fn;
 }
 
-// 2-D tensor map over W_UK_T viewed as [H*128 rows][512 columns]; one box is
-// the 128 x 64 tile a CTA owns.  BF16 tiles land 128B-swizzled (the layout
-// the kernel's ldmatrix addressing expects); E4M3 tiles land unswizzled.
-int encode_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
+// 2-D tensor map over W_UK_T viewed as [H*K rows][512 columns]; one box is
+// the K x 64 tile a CTA owns.  BF16 tiles land 128B-swizzled (the layout the
+// kernel's ldmatrix addressing expects); E4M3 tiles land unswizzled.
+int encode_weight_map(CUtensorMap* map, const void* weight, int H, int K, bool mx) {
   std::string err;
   EncodeTiledFn fn = encode_tiled_fn(&err);
   if (!fn) return fail(MLAQP_ERR_CUDA, err);
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM), static_cast<cuuint64_t>(H) * MLAQP_NOPE_DIM};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM), static_cast<cuuint64_t>(H) * K};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM) * (mx ? 1 : 2)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(mlaqp::kNTile), static_cast<cuuint32_t>(MLAQP_NOPE_DIM)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(mlaqp::kNTile), static_cast<cuuint32_t>(K)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                         const_cast<void*>(weight), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -189,26 +189,37 @@ int smem_for_cap(const DeviceInfo& d, int base, int cap) {
   return bytes > base ? (bytes < d.max_smem_optin ? bytes : d.max_smem_optin) : base;
 }
 
-int policy_max_smem(const DeviceInfo& d) { return smem_for_cap(d, mlaqp::kSmemBytes, 3); }
+int policy_max_smem(const DeviceInfo& d) {
+  const int base = mlaqp::Smem<128>::Bytes > mlaqp::Smem<192>::Bytes ? mlaqp::Smem<128>::Bytes : mlaqp::Smem<192>::Bytes;
+  return smem_for_cap(d, base, 3);
+}
 
-const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig) {
+// Index of a supported nope dim in the kernel tables, or -1.
+int nope_index(int K) {
+  for (int i = 0; i < 2; ++i)
+    if (mlaqp::kNopeDims[i] == K) return i;
+  return -1;
+}
+
+const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int nope_idx) {
   const int mt = (M + 7) / 8;
   if (mt < 1 || mt > 4) return nullptr;
   const mlaqp::KernelTable& table =
       weight_format == MLAQP_WEIGHT_BF16 ? mlaqp::kernels_bf16_weights() : mlaqp::kernels_mxfp8_weights();
-  return &table[out_dtype][mt - 1][trig];
+  return &table[nope_idx][out_dtype][mt - 1][trig];
 }
 
 int setup_kernels(const DeviceInfo& d) {
   const int smem = policy_max_smem(d);
-  for (int wf = 0; wf < 2; ++wf)
-    for (int od = 0; od < 2; ++od)
-      for (int mt = 1; mt <= 4; ++mt)
-        for (int trig = 0; trig < mlaqp::kTrigVariants; ++trig) {
-          const KernelInfo* k = lookup(wf, od, 8 * mt, trig);
-          const cudaError_t e = cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-          if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
-        }
+  for (int ki = 0; ki < 2; ++ki)
+    for (int wf = 0; wf < 2; ++wf)
+      for (int od = 0; od < 2; ++od)
+        for (int mt = 1; mt <= 4; ++mt)
+          for (int trig = 0; trig < mlaqp::kTrigVariants; ++trig) {
+            const KernelInfo* k = lookup(wf, od, 8 * mt, trig, ki);
+            const cudaError_t e = cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+          }
   return MLAQP_OK;
 }
 
@@ -230,41 +241,73 @@ Range span(const void* p, size_t bytes) {
   return Range{lo, lo + bytes};
 }
 
-int run_impl(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
-             int64_t out_row_stride, const float* q_scale, int M, int H, int weight_format, int out_dtype,
-             mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
-  if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format or out_dtype");
+// One layer call's arguments (pointers as given by the caller, strides in
+// elements).
+struct RunArgs {
+  const void* q_nope;
+  int64_t q_nope_ts, q_nope_hs;
+  const void* q_pe;
+  int64_t q_pe_ts, q_pe_hs;
+  const void* weight;
+  const void* weight_scale;
+  void* out;
+  int64_t out_row_stride;
+  const float* q_scale;
+  int M, H, K, weight_format, out_dtype;
+};
+
+RunArgs contiguous_args(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
+                        int64_t out_row_stride, const float* q_scale, int M, int H, int weight_format, int out_dtype) {
+  return RunArgs{q_nope, static_cast<int64_t>(H) * MLAQP_NOPE_DIM, MLAQP_NOPE_DIM,
+                 q_pe, static_cast<int64_t>(H) * MLAQP_ROPE_DIM, MLAQP_ROPE_DIM,
+                 weight, weight_scale, out, out_row_stride, q_scale, M, H, MLAQP_NOPE_DIM, weight_format, out_dtype};
+}
+
+int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
+  const int M = a.M, H = a.H, K = a.K;
+  if (!valid_enums(a.weight_format, a.out_dtype)) return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format or out_dtype");
   if (M < 0) return fail(MLAQP_ERR_INVALID_ARG, "M must be >= 0");
   if (!supported_heads(H)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
   if (M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "M must be <= 32");
+  const int ki = nope_index(K);
+  if (ki < 0) return fail(MLAQP_ERR_UNSUPPORTED, "nope_dim must be 128 or 192");
   if (M == 0) return MLAQP_OK;
 
-  const bool mx = weight_format == MLAQP_WEIGHT_MXFP8;
-  const bool e4m3 = out_dtype == MLAQP_OUT_E4M3;
-  if (!q_nope || !q_pe || !weight || !out) return fail(MLAQP_ERR_INVALID_ARG, "q_nope, q_pe, weight and out are required");
-  if (mx && !weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "MXFP8 weights require weight_scale");
-  if (!mx && weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 weights take no weight_scale (pass NULL)");
-  if (e4m3 && !q_scale) return fail(MLAQP_ERR_INVALID_ARG, "E4M3 output requires q_scale");
-  if (!e4m3 && q_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 output takes no q_scale (pass NULL)");
-  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(weight, 16) || !aligned(out, 16) ||
-      (weight_scale && !aligned(weight_scale, 16)) || (q_scale && !aligned(q_scale, 4)))
-    return fail(MLAQP_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (q_scale 4-byte)");
+  const bool mx = a.weight_format == MLAQP_WEIGHT_MXFP8;
+  const bool e4m3 = a.out_dtype == MLAQP_OUT_E4M3;
+  if (!a.q_nope || !a.q_pe || !a.weight || !a.out)
+    return fail(MLAQP_ERR_INVALID_ARG, "q_nope, q_pe, weight and out are required");
+  if (mx && !a.weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "MXFP8 weights require weight_scale");
+  if (!mx && a.weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 weights take no weight_scale (pass NULL)");
+  if (e4m3 && !a.q_scale) return fail(MLAQP_ERR_INVALID_ARG, "E4M3 output requires q_scale");
+  if (!e4m3 && a.q_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 output takes no q_scale (pass NULL)");
+  if (!aligned(a.q_nope, 16) || !aligned(a.weight, 16) || !aligned(a.out, 16) ||
+      (a.weight_scale && !aligned(a.weight_scale, 16)))
+    return fail(MLAQP_ERR_INVALID_ARG, "q_nope, weight, weight_scale and out must be 16-byte aligned");
+  if (!aligned(a.q_pe, 4) || (a.q_scale && !aligned(a.q_scale, 4)))
+    return fail(MLAQP_ERR_INVALID_ARG, "q_pe and q_scale must be 4-byte aligned");
+  if (a.q_nope_ts < 0 || a.q_nope_hs < 0 || a.q_pe_ts < 0 || a.q_pe_hs < 0)
+    return fail(MLAQP_ERR_INVALID_ARG, "input strides must be >= 0");
+  if (a.q_nope_ts % 8 != 0 || a.q_nope_hs % 8 != 0)
+    return fail(MLAQP_ERR_INVALID_ARG, "q_nope strides must be multiples of 8 elements (16 bytes)");
+  if (a.q_pe_ts % 2 != 0 || a.q_pe_hs % 2 != 0)
+    return fail(MLAQP_ERR_INVALID_ARG, "q_pe strides must be multiples of 2 elements (4 bytes)");
   const int64_t out_elem = e4m3 ? 1 : 2;
-  if (out_row_stride < static_cast<int64_t>(MLAQP_OUT_DIM) * H)
+  if (a.out_row_stride < static_cast<int64_t>(MLAQP_OUT_DIM) * H)
     return fail(MLAQP_ERR_INVALID_ARG, "out_row_stride must be >= 576*H elements");
-  if ((out_row_stride * out_elem) % 16 != 0)
+  if ((a.out_row_stride * out_elem) % 16 != 0)
     return fail(MLAQP_ERR_INVALID_ARG, "out_row_stride * element size must be a multiple of 16 bytes");
 
-  const size_t out_bytes =
-      static_cast<size_t>((static_cast<int64_t>(M - 1) * out_row_stride + static_cast<int64_t>(MLAQP_OUT_DIM) * H) * out_elem);
-  const Range o = span(out, out_bytes);
-  const size_t w_elems = static_cast<size_t>(H) * MLAQP_NOPE_DIM * MLAQP_LATENT_DIM;
+  const size_t out_bytes = static_cast<size_t>(
+      (static_cast<int64_t>(M - 1) * a.out_row_stride + static_cast<int64_t>(MLAQP_OUT_DIM) * H) * out_elem);
+  const Range o = span(a.out, out_bytes);
+  const size_t w_elems = static_cast<size_t>(H) * K * MLAQP_LATENT_DIM;
   const Range inputs[5] = {
-      span(q_nope, static_cast<size_t>(M) * H * MLAQP_NOPE_DIM * 2),
-      span(q_pe, static_cast<size_t>(M) * H * MLAQP_ROPE_DIM * 2),
-      span(weight, w_elems * (mx ? 1 : 2)),
-      span(weight_scale, mx ? w_elems / 32 : 0),
-      span(q_scale, e4m3 ? sizeof(float) : 0),
+      span(a.q_nope, static_cast<size_t>((M - 1) * a.q_nope_ts + (H - 1) * a.q_nope_hs + K) * 2),
+      span(a.q_pe, static_cast<size_t>((M - 1) * a.q_pe_ts + (H - 1) * a.q_pe_hs + MLAQP_ROPE_DIM) * 2),
+      span(a.weight, w_elems * (mx ? 1 : 2)),
+      span(a.weight_scale, mx ? w_elems / 32 : 0),
+      span(a.q_scale, e4m3 ? sizeof(float) : 0),
   };
   for (const Range& r : inputs)
     if (r.hi > r.lo && overlaps(o, r)) return fail(MLAQP_ERR_INVALID_ARG, "out overlaps an input tensor");
@@ -275,18 +318,22 @@ int run_impl(const void* q_nope, const void* q_pe, const void* weight, const voi
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  const LaunchPolicy pol = launch_policy(weight_format, M);
-  const KernelInfo* k = lookup(weight_format, out_dtype, M, pol.trig);
+  const LaunchPolicy pol = launch_policy(a.weight_format, M);
+  const KernelInfo* k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki);
   const int smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   RunParams params;
-  st = encode_weight_map(&params.wmap, weight, H, mx);
+  st = encode_weight_map(&params.wmap, a.weight, H, K, mx);
   if (st != MLAQP_OK) return st;
-  params.q_nope = static_cast<const uint16_t*>(q_nope);
-  params.q_pe = static_cast<const uint16_t*>(q_pe);
-  params.weight_scale = static_cast<const uint8_t*>(weight_scale);
-  params.out = static_cast<uint8_t*>(out);
-  params.out_row_stride = out_row_stride;
-  params.q_scale = q_scale;
+  params.q_nope = static_cast<const uint16_t*>(a.q_nope);
+  params.q_pe = static_cast<const uint16_t*>(a.q_pe);
+  params.q_nope_ts = a.q_nope_ts;
+  params.q_nope_hs = a.q_nope_hs;
+  params.q_pe_ts = a.q_pe_ts;
+  params.q_pe_hs = a.q_pe_hs;
+  params.weight_scale = static_cast<const uint8_t*>(a.weight_scale);
+  params.out = static_cast<uint8_t*>(a.out);
+  params.out_row_stride = a.out_row_stride;
+  params.q_scale = a.q_scale;
   params.wait_limit_ns = wait_limit_ns;
   params.extra_tx = extra_tx;
   params.M = M;
@@ -319,8 +366,8 @@ int mlaqp_can_implement(int num_heads, int max_m, int nope_dim, int latent_dim, 
   if (!valid_enums(weight_format, out_dtype)) return fail(0, "unknown weight_format or out_dtype");
   if (!supported_heads(num_heads)) return fail(0, "num_heads must be 8, 11 or 16");
   if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(0, "max_m must be in 1..32");
-  if (nope_dim != MLAQP_NOPE_DIM || latent_dim != MLAQP_LATENT_DIM || rope_dim != MLAQP_ROPE_DIM)
-    return fail(0, "only nope_dim=128, latent_dim=512, rope_dim=64 are implemented");
+  if (nope_index(nope_dim) < 0 || latent_dim != MLAQP_LATENT_DIM || rope_dim != MLAQP_ROPE_DIM)
+    return fail(0, "only nope_dim 128 or 192, latent_dim 512 and rope_dim 64 are implemented");
   int dev = 0;
   if (resolve_device(device, &dev) != MLAQP_OK) return 0;
   int count = 0;
@@ -350,12 +397,13 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
   for (int mt = 1; mt <= (max_m + 7) / 8 && status == MLAQP_OK; ++mt) {
     const uint32_t bit = 1u << (((weight_format * 2 + out_dtype) * 4) + (mt - 1));
     if (g_prewarmed[dev].load(std::memory_order_acquire) & bit) continue;
-    for (int trig = 0; trig < mlaqp::kTrigVariants && status == MLAQP_OK; ++trig) {
-      const KernelInfo* k = lookup(weight_format, out_dtype, 8 * mt, trig);
-      cudaFuncAttributes attr;
-      e = cudaFuncGetAttributes(&attr, k->fn);  // forces the kernel image to load
-      if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
-    }
+    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)
+      for (int trig = 0; trig < mlaqp::kTrigVariants && status == MLAQP_OK; ++trig) {
+        const KernelInfo* k = lookup(weight_format, out_dtype, 8 * mt, trig, ki);
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, k->fn);  // forces the kernel image to load
+        if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
+      }
     if (status != MLAQP_OK) break;
     g_prewarmed[dev].fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -366,21 +414,32 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
 int mlaqp_run(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
               int64_t out_row_stride, const float* q_scale, int M, int H, int weight_format, int out_dtype,
               mlaqp_stream_t stream) {
-  return run_impl(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H, weight_format, out_dtype,
+  return run_impl(contiguous_args(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H,
+                                  weight_format, out_dtype),
                   stream, false, kDefaultWaitLimitNs, 0);
 }
 
 int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
                   int64_t out_row_stride, const float* q_scale, int M, int H, int weight_format, int out_dtype,
                   mlaqp_stream_t stream) {
-  return run_impl(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H, weight_format, out_dtype,
+  return run_impl(contiguous_args(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H,
+                                  weight_format, out_dtype),
                   stream, true, kDefaultWaitLimitNs, 0);
+}
+
+int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride, const void* q_pe,
+                      int64_t q_pe_token_stride, int64_t q_pe_head_stride, const void* weight,
+                      const void* weight_scale, void* out, int64_t out_row_stride, const float* q_scale, int M,
+                      int H, int nope_dim, int weight_format, int out_dtype, int pdl, mlaqp_stream_t stream) {
+  const RunArgs a{q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_pe_token_stride, q_pe_head_stride,
+                  weight, weight_scale, out, out_row_stride, q_scale, M, H, nope_dim, weight_format, out_dtype};
+  return run_impl(a, stream, pdl != 0, kDefaultWaitLimitNs, 0);
 }
 
 int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas, int* threads_per_cta) {
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
-  const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, M).trig);
+  const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, M).trig, 0);
   if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
   if (threads_per_cta) *threads_per_cta = k->threads;
   return MLAQP_OK;
@@ -392,7 +451,8 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
                                  unsigned int extra_tx_bytes, mlaqp_stream_t stream) {
   if (wait_limit_ns == 0) return fail(MLAQP_ERR_INVALID_ARG, "wait_limit_ns must be > 0");
   if (extra_tx_bytes > (1u << 19)) return fail(MLAQP_ERR_INVALID_ARG, "extra_tx_bytes must be <= 2^19");
-  return run_impl(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H, weight_format, out_dtype,
+  return run_impl(contiguous_args(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H,
+                                  weight_format, out_dtype),
                   stream, false, wait_limit_ns, extra_tx_bytes);
 }
 

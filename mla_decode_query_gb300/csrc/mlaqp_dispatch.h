@@ -13,11 +13,13 @@ struct KernelInfo {
   int smem_bytes;      // dynamic shared memory per CTA
 };
 
-// Table [out_dtype][mt-1][trig], mt = ceil(M/8) in 1..4, trig = where the
-// CTA triggers the next kernel's launch (0: at entry, 1: after the
-// dependency wait, 2: once its weight tile is ready).
+// Table [nope][out_dtype][mt-1][trig]: nope 0 = K 128, 1 = K 192;
+// mt = ceil(M/8) in 1..4; trig = where the CTA triggers the next kernel's
+// launch (0: at entry, 1: after the dependency wait, 2: once its weight
+// tile is ready).
 constexpr int kTrigVariants = 3;
-using KernelTable = KernelInfo[2][4][kTrigVariants];
+constexpr int kNopeDims[2] = {128, 192};
+using KernelTable = KernelInfo[2][2][4][kTrigVariants];
 
 const KernelTable& kernels_bf16_weights();
 const KernelTable& kernels_mxfp8_weights();

@@ -46,7 +46,7 @@
 
 namespace mlaqp {
 
-constexpr int kNope = 128;
+constexpr int kNope = 128;     // nope dim of the benchmark configurations; 192 is also built
 constexpr int kLatent = 512;
 constexpr int kRope = 64;
 constexpr int kOutDim = kLatent + kRope;
@@ -63,14 +63,19 @@ constexpr int kThreads = kWarps * 32;            // 128 threads per token group
 constexpr int token_groups(int mt) { return mt >= 2 ? 2 : 1; }
 constexpr int kTilesPerHead = kLatent / kNTile;  // 8
 
-// Dynamic shared memory layout (offsets from a 1024-byte aligned base).
-constexpr int kSmemA = 0;                            // BF16 [128][64], 128B swizzle: 16 KB
-constexpr int kSmemRaw = kSmemA + kNope * kNTile * 2;  // E4M3 [128][64]: 8 KB
-constexpr int kSmemScale = kSmemRaw + kNope * kNTile;  // E8M0 [128][16]: 2 KB
-constexpr int kSmemQ = kSmemScale + kNope * (kLatent / kMxBlock);  // BF16 [32][128], 16B chunks XOR-swizzled: 8 KB
-constexpr int kSmemDiv = kSmemQ + kMaxM * kNope * 2;  // FP32 [128]: RN((128+f)/q_scale)
-constexpr int kSmemBar = kSmemDiv + 128 * 4;
-constexpr int kSmemBytes = kSmemBar + 64 + 1024;  // + slack for the 1024-byte alignment
+// Dynamic shared memory layout for nope dim K (offsets from a 1024-byte
+// aligned base; every region starts on at least a 16-byte boundary).
+template <int K>
+struct Smem {
+  static constexpr int A = 0;                                 // BF16 [K][64], 128B swizzle
+  static constexpr int Raw = A + K * kNTile * 2;              // E4M3 [K][64]
+  static constexpr int Scale = Raw + K * kNTile;              // E8M0 [K][16]
+  static constexpr int Q = Scale + K * (kLatent / kMxBlock);  // BF16 [32][K], 16B chunks XOR-swizzled
+  static constexpr int Div = Q + kMaxM * K * 2;               // FP32 [128]: RN((128+f)/q_scale)
+  static constexpr int Bar = Div + 128 * 4;
+  static constexpr int Bytes = Bar + 64 + 1024;               // + slack for the 1024-byte alignment
+};
+constexpr int kSmemBytes = Smem<kNope>::Bytes;
 
 enum WeightFormat : int { kWeightBF16 = 0, kWeightMXFP8 = 1 };
 enum OutDtype : int { kOutBF16 = 0, kOutE4M3 = 1 };
@@ -79,8 +84,10 @@ constexpr unsigned kDevStatusWaitTimeout = 1u;
 
 struct RunParams {
   CUtensorMap wmap;             // 2-D map of W_UK_T viewed as [H*128 rows][512 cols], box 64 x 128
-  const uint16_t* q_nope;       // BF16 [M,H,128]
-  const uint16_t* q_pe;         // BF16 [M,H,64]
+  const uint16_t* q_nope;       // BF16, element (m,h,k) at m*q_nope_ts + h*q_nope_hs + k
+  const uint16_t* q_pe;         // BF16, element (m,h,j) at m*q_pe_ts + h*q_pe_hs + j
+  int64_t q_nope_ts, q_nope_hs; // token / head strides (elements)
+  int64_t q_pe_ts, q_pe_hs;
   const uint8_t* weight_scale;  // E8M0 [H,128,16] or null
   uint8_t* out;                 // element (m,h,j) at m*out_row_stride + h*576 + j
   int64_t out_row_stride;       // elements
@@ -317,11 +324,13 @@ __device__ __forceinline__ uint32_t e4m3_pair(uint32_t two_bf16, const uint32_t*
   }
 }
 
-// Byte offset of 16-byte chunk `chunk` (0..15) of token row `m` in the
-// q_nope tile of 256-byte rows; XOR with m mod 8 makes the eight rows an
-// ldmatrix reads hit eight different bank groups.
+// Byte offset of 16-byte chunk `chunk` (0..K/8-1) of token row `m` in the
+// q_nope tile of 2K-byte rows (a multiple of 128 bytes); XOR of the low
+// three chunk bits with m mod 8 makes the eight rows an ldmatrix reads hit
+// eight different bank groups.
+template <int K>
 __device__ __forceinline__ uint32_t q_off(int m, int chunk) {
-  return static_cast<uint32_t>(m * 256 + ((chunk ^ (m & 7)) << 4));
+  return static_cast<uint32_t>(m * (2 * K) + ((chunk ^ (m & 7)) << 4));
 }
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a tile of 128-byte
@@ -395,14 +404,18 @@ __device__ __forceinline__ void write_pe_pair(const RunParams& p, size_t off, ui
 //   2 = once its weight tile is in shared memory (MXFP8: dequantised).
 // ---------------------------------------------------------------------------
 
-template <int WF, int OD, int MT, int TRIG, int TS = token_groups(MT)>
+template <int WF, int OD, int MT, int TRIG, int K, int TS = token_groups(MT)>
 __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const __grid_constant__ RunParams p) {
+  static_assert(K % 32 == 0 && K <= 256, "nope dim: multiple of 32, at most one TMA box (256 rows)");
+  using L = Smem<K>;
   constexpr int kCta = kThreads * TS;       // threads in the CTA
   constexpr int MTW = (MT + TS - 1) / TS;   // token tiles per warp
+  constexpr int KS = K / 16;                // MMA k-steps
+  constexpr int KC = K / 8;                 // 16-byte chunks per q_nope row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t s_a = smem_u32(smem + kSmemA);
-  const uint32_t s_bar = smem_u32(smem + kSmemBar);
+  const uint32_t s_a = smem_u32(smem + L::A);
+  const uint32_t s_bar = smem_u32(smem + L::Bar);
 
   const int tile = blockIdx.x;
   const int h = blockIdx.y;
@@ -429,13 +442,13 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     mbar_init(s_bar, 1);
     fence_barrier_init();
     if constexpr (WF == kWeightBF16) {
-      mbar_arrive_expect_tx(s_bar, kNope * kNTile * 2 + p.extra_tx);
-      tma_load_2d(s_a, &p.wmap, n_cta, h * kNope, s_bar);
+      mbar_arrive_expect_tx(s_bar, K * kNTile * 2 + p.extra_tx);
+      tma_load_2d(s_a, &p.wmap, n_cta, h * K, s_bar);
     } else {
-      mbar_arrive_expect_tx(s_bar, kNope * kNTile + kNope * (kLatent / kMxBlock) + p.extra_tx);
-      tma_load_2d(smem_u32(smem + kSmemRaw), &p.wmap, n_cta, h * kNope, s_bar);
-      bulk_load_1d(smem_u32(smem + kSmemScale), p.weight_scale + static_cast<size_t>(h) * kNope * (kLatent / kMxBlock),
-                   kNope * (kLatent / kMxBlock), s_bar);
+      mbar_arrive_expect_tx(s_bar, K * kNTile + K * (kLatent / kMxBlock) + p.extra_tx);
+      tma_load_2d(smem_u32(smem + L::Raw), &p.wmap, n_cta, h * K, s_bar);
+      bulk_load_1d(smem_u32(smem + L::Scale), p.weight_scale + static_cast<size_t>(h) * K * (kLatent / kMxBlock),
+                   K * (kLatent / kMxBlock), s_bar);
     }
   }
 
@@ -443,28 +456,28 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   //    fetched before the producer writes it is updated by that write; the
   //    values themselves are read only after the dependency wait).
   if (warp == 0 && lane < M) {
-    const uint16_t* qrow = p.q_nope + (static_cast<size_t>(lane) * H + h) * kNope;
-    prefetch_l2(qrow);
-    prefetch_l2(qrow + 64);
-    prefetch_l2(p.q_pe + (static_cast<size_t>(lane) * H + h) * kRope);
+    const uint16_t* qrow = p.q_nope + lane * p.q_nope_ts + h * p.q_nope_hs;
+#pragma unroll
+    for (int o = 0; o < K; o += 64) prefetch_l2(qrow + o);
+    prefetch_l2(p.q_pe + lane * p.q_pe_ts + h * p.q_pe_hs);
   }
   __syncthreads();  // barrier initialised before anyone waits on it
 
   // 3. MXFP8: dequantise into the swizzled BF16 tile before the dependency
-  //    wait.  Job (row k, chunk c of 8 columns); 1024 jobs, 8/TS per thread.
+  //    wait.  Job (row k, chunk c of 8 columns); 8K jobs, 8K/(128 TS) per thread.
   if constexpr (WF == kWeightMXFP8) {
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
       return;
     }
-    const uint8_t* raw = smem + kSmemRaw;
-    const uint8_t* sc = smem + kSmemScale;
+    const uint8_t* raw = smem + L::Raw;
+    const uint8_t* sc = smem + L::Scale;
     const int c = tid & 7;
     const int blk = (n_cta + 8 * c) / kMxBlock;
     // Loads of all jobs first, then the arithmetic, then the stores: the
     // phases keep every job's chain independent of the others' stores.
-    constexpr int kJobs = 8 / TS;
+    constexpr int kJobs = 8 * K / kCta;
     uint2 v[kJobs];
     uint32_t xs[kJobs];
 #pragma unroll
@@ -492,7 +505,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
 #pragma unroll
     for (int i = 0; i < kJobs; ++i) {
       const int k = (tid >> 3) + (kCta / 8) * i;
-      *reinterpret_cast<uint4*>(smem + kSmemA + sw128(k, c)) = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
+      *reinterpret_cast<uint4*>(smem + L::A + sw128(k, c)) = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
     }
     __syncthreads();
     if constexpr (TRIG == 2) pdl_launch_dependents();
@@ -507,7 +520,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
 
   // E4M3 output: table of RN((128+f)/q_scale), one entry per thread, made
   // visible by the barrier after the q_nope tile is stored.
-  uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + kSmemDiv);
+  uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L::Div);
   bool table_ok = false;
   if constexpr (OD == kOutE4M3) {
     table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
@@ -526,16 +539,16 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   const bool has_pe = j_pe < M * (kRope / 2);
   const int m_pe = j_pe >> 5;
   uint32_t pe = 0u;
-  if (has_pe) pe = ld_u32(p.q_pe + (static_cast<size_t>(m_pe) * H + h) * kRope + 2 * (j_pe & 31));
-  constexpr int kQChunks = 128 * MT;  // 16-byte chunks of the [8*MT][128] tile
+  if (has_pe) pe = ld_u32(p.q_pe + m_pe * p.q_pe_ts + h * p.q_pe_hs + 2 * (j_pe & 31));
+  constexpr int kQChunks = 8 * MT * KC;  // 16-byte chunks of the [8*MT][K] tile
   constexpr int QI = (kQChunks + kCta - 1) / kCta;
   uint4 qv[QI];
 #pragma unroll
   for (int i = 0; i < QI; ++i) {
-    const int c = tid + kCta * i;  // chunk c: token row c/16, k chunk c%16
-    const int m = c >> 4;
+    const int c = tid + kCta * i;  // chunk c: token row c/KC, k chunk c%KC
+    const int m = c / KC;
     qv[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (c < kQChunks && m < M) qv[i] = ld_u128(p.q_nope + (static_cast<size_t>(m) * H + h) * kNope + 8 * (c & 15));
+    if (c < kQChunks && m < M) qv[i] = ld_u128(p.q_nope + m * p.q_nope_ts + h * p.q_nope_hs + 8 * (c % KC));
   }
 
   if constexpr (WF == kWeightBF16 && TRIG != 2) {
@@ -550,14 +563,14 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   // 2/3 = k 16s+8..+15; 0/2 = columns 16w..+7, 1/3 = 16w+8..+15.
   const int mi = lane >> 3;
   const int chunk = 2 * wcol + (mi & 1);
-  uint32_t a[8][4];
+  uint32_t a[KS][4];
 #pragma unroll
-  for (int s = 0; s < 8; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
+  for (int s = 0; s < KS; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
 
 #pragma unroll
   for (int i = 0; i < QI; ++i) {
     const int c = tid + kCta * i;
-    if (c < kQChunks) *reinterpret_cast<uint4*>(smem + kSmemQ + q_off(c >> 4, c & 15)) = qv[i];
+    if (c < kQChunks) *reinterpret_cast<uint4*>(smem + L::Q + q_off<K>(c / KC, c % KC)) = qv[i];
   }
   __syncthreads();
 
@@ -576,23 +589,23 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   //    over this warp's token tiles jt = wtok + TS*i.  B (q_nope): matrix L>>3
   //    of ldmatrix is k chunk 4*s2 + (L>>3) of tokens 8jt..8jt+7, giving
   //    b0/b1 of steps 2*s2 and 2*s2+1.
-  const uint32_t s_q = smem_u32(smem + kSmemQ);
+  const uint32_t s_q = smem_u32(smem + L::Q);
   bool tile_ok[MTW];
 #pragma unroll
   for (int i = 0; i < MTW; ++i) tile_ok[i] = wtok + TS * i < MT;  // uniform per warp
-  uint32_t b[4][MTW][4];
+  uint32_t b[KS / 2][MTW][4];
 #pragma unroll
-  for (int s2 = 0; s2 < 4; ++s2)
+  for (int s2 = 0; s2 < KS / 2; ++s2)
 #pragma unroll
     for (int i = 0; i < MTW; ++i)
-      if (tile_ok[i]) ldmatrix_x4(b[s2][i], s_q + q_off(8 * (wtok + TS * i) + (lane & 7), 4 * s2 + mi));
+      if (tile_ok[i]) ldmatrix_x4(b[s2][i], s_q + q_off<K>(8 * (wtok + TS * i) + (lane & 7), 4 * s2 + mi));
   float acc[2][MTW][4];
 #pragma unroll
   for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
     for (int i = 0; i < MTW; ++i) acc[c2][i][0] = acc[c2][i][1] = acc[c2][i][2] = acc[c2][i][3] = 0.f;
 #pragma unroll
-  for (int s = 0; s < 8; ++s)
+  for (int s = 0; s < KS; ++s)
 #pragma unroll
     for (int i = 0; i < MTW; ++i)
       if (tile_ok[i]) mma_bf16_16816(acc[s & 1][i], a[s], b[s >> 1][i][2 * (s & 1)], b[s >> 1][i][2 * (s & 1) + 1]);

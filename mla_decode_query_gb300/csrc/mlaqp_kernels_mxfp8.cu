@@ -6,27 +6,43 @@ namespace mlaqp {
 namespace {
 constexpr int kWF = kWeightMXFP8;
 
-template <int OD, int MT, int TRIG>
+template <int K, int OD, int MT, int TRIG>
 KernelInfo entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT, TRIG>), kThreads * token_groups(MT),
-                    kTilesPerHead, kSmemBytes};
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT, TRIG, K>),
+                    kThreads * token_groups(MT), kTilesPerHead, Smem<K>::Bytes};
 }
 
+template <int K, int OD, int MT>
+void fill(KernelInfo (&row)[kTrigVariants]) {
+  row[0] = entry<K, OD, MT, 0>();
+  row[1] = entry<K, OD, MT, 1>();
+  row[2] = entry<K, OD, MT, 2>();
+}
 
+template <int K>
+void fill_nope(KernelInfo (&t)[2][4][kTrigVariants]) {
+  fill<K, kOutBF16, 1>(t[0][0]);
+  fill<K, kOutBF16, 2>(t[0][1]);
+  fill<K, kOutBF16, 3>(t[0][2]);
+  fill<K, kOutBF16, 4>(t[0][3]);
+  fill<K, kOutE4M3, 1>(t[1][0]);
+  fill<K, kOutE4M3, 2>(t[1][1]);
+  fill<K, kOutE4M3, 3>(t[1][2]);
+  fill<K, kOutE4M3, 4>(t[1][3]);
+}
+
+struct Table {
+  KernelTable t;
+  Table() {
+    fill_nope<128>(t[0]);
+    fill_nope<192>(t[1]);
+  }
+};
 }  // namespace
 
 const KernelTable& kernels_mxfp8_weights() {
-  static const KernelTable table = {
-      {{entry<kOutBF16, 1, 0>(), entry<kOutBF16, 1, 1>(), entry<kOutBF16, 1, 2>()},
-       {entry<kOutBF16, 2, 0>(), entry<kOutBF16, 2, 1>(), entry<kOutBF16, 2, 2>()},
-       {entry<kOutBF16, 3, 0>(), entry<kOutBF16, 3, 1>(), entry<kOutBF16, 3, 2>()},
-       {entry<kOutBF16, 4, 0>(), entry<kOutBF16, 4, 1>(), entry<kOutBF16, 4, 2>()}},
-      {{entry<kOutE4M3, 1, 0>(), entry<kOutE4M3, 1, 1>(), entry<kOutE4M3, 1, 2>()},
-       {entry<kOutE4M3, 2, 0>(), entry<kOutE4M3, 2, 1>(), entry<kOutE4M3, 2, 2>()},
-       {entry<kOutE4M3, 3, 0>(), entry<kOutE4M3, 3, 1>(), entry<kOutE4M3, 3, 2>()},
-       {entry<kOutE4M3, 4, 0>(), entry<kOutE4M3, 4, 1>(), entry<kOutE4M3, 4, 2>()}},
-  };
-  return table;
+  static const Table table;
+  return table.t;
 }
 
 cudaError_t device_status_mxfp8_weights(unsigned int* value, bool reset) { return read_device_status(value, reset); }
