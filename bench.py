@@ -40,11 +40,11 @@ Q_SCALE_SEED = 3
 L2_BYTES = 126 * 2**20
 
 
-def algorithmic_bytes(M, weight_format, out_dtype, h=H):
+def algorithmic_bytes(M, weight_format, out_dtype, h=H, nope=128):
     wb = 2 if weight_format == "bf16" else 1
     ob = 2 if out_dtype == "bf16" else 1
-    scales = h * 128 * 16 if weight_format == "mxfp8" else 0
-    return h * 128 * 512 * wb + scales + 2 * M * h * 128 + 2 * M * h * 64 + M * h * 576 * ob
+    scales = h * nope * 16 if weight_format == "mxfp8" else 0
+    return h * nope * 512 * wb + scales + 2 * M * h * nope + 2 * M * h * 64 + M * h * 576 * ob
 
 
 # --------------------------------------------------------------------------- device layer sets
@@ -54,14 +54,14 @@ class LayerSet:
     and output buffers laid out [L, M, H, *] so each launch reads its own."""
 
     def __init__(self, weight_format, out_dtype, n_layers, h=H, m_points=M_POINTS, device="cuda",
-                 config_index=None):
+                 config_index=None, nope=128):
         import torch
         from mla_decode_query_gb300 import inputs
 
-        self.weight_format, self.out_dtype, self.L, self.H = weight_format, out_dtype, n_layers, h
+        self.weight_format, self.out_dtype, self.L, self.H, self.K = weight_format, out_dtype, n_layers, h, nope
         self.m_points = tuple(m_points)
         ci = CONFIG_INDEX[weight_format] if config_index is None else config_index
-        self.host = [inputs.make_layer(inputs.layer_seed(ci, l), h, weight_format) for l in range(n_layers)]
+        self.host = [inputs.make_layer(inputs.layer_seed(ci, l), h, weight_format, nope=nope) for l in range(n_layers)]
         wdt = torch.int16 if weight_format == "bf16" else torch.uint8
         w = np.stack([d["weight"] for d in self.host])
         self.weight = torch.from_numpy(w.view(np.int16) if weight_format == "bf16" else w).to(device)
@@ -91,6 +91,14 @@ class LayerSet:
 
     def launch_all(self, M, pdl=True, stream=None):
         import mla_decode_query_gb300 as mq
+        if self.K != 128:  # the general entry point: nope dim and (contiguous) strides
+            for l in range(self.L):
+                a = self.layer_args(M, l)
+                mq.check(mq.mlaqp_run_strided(a["q_nope"], self.H * self.K, self.K, a["q_pe"], self.H * 64, 64,
+                                              a["weight"], a["weight_scale"], a["out"], a["out_row_stride"],
+                                              a["q_scale"], M, self.H, self.K, self.weight_format, self.out_dtype,
+                                              pdl=pdl, stream=stream))
+            return
         run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
         for l in range(self.L):
             mq.check(run(**self.layer_args(M, l), stream=stream))
@@ -111,7 +119,7 @@ class LayerSet:
         return g
 
     def bytes_per_call(self, M):
-        return algorithmic_bytes(M, self.weight_format, self.out_dtype, self.H)
+        return algorithmic_bytes(M, self.weight_format, self.out_dtype, self.H, self.K)
 
 
 # --------------------------------------------------------------------------- clocks
@@ -278,7 +286,7 @@ def run_gpu(args):
     sets = []
     for fmt, od in formats:
         L = args.layers or DEFAULT_LAYERS[fmt]
-        sets.append(LayerSet(fmt, od, L, m_points=m_points))
+        sets.append(LayerSet(fmt, od, L, m_points=m_points, nope=args.nope))
     points = [(s, M) for s in sets for M in m_points]
     graphs = [s.capture(M, pdl=not args.no_pdl) for s, M in points]
     alt = None
@@ -370,7 +378,8 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "heads": H, "m_points": list(m_points),
+            "config": {"workload": WORKLOAD if args.nope == 128 else WORKLOAD.replace("K=128", f"K={args.nope}"),
+                       "heads": H, "nope_dim": args.nope, "m_points": list(m_points),
                        "layers": {s.weight_format: s.L for s in sets}, "pdl": not args.no_pdl,
                        "l2": f"rotated weights per replay {[s.L * s.bytes_per_call(1) >> 20 for s in sets]} MiB "
                              f"vs L2 {L2_BYTES >> 20} MiB (inputs larger than L2, no flush)",
@@ -509,6 +518,7 @@ def main(argv=None):
     ap.add_argument("--m", type=str, default="", help="comma-separated token counts")
     ap.add_argument("--formats", type=str, default="", help="comma-separated subset of bf16,mxfp8")
     ap.add_argument("--pairs", type=str, default="", help="comma-separated weight:output pairs, e.g. bf16:e4m3")
+    ap.add_argument("--nope", type=int, default=128, choices=(128, 192), help="nope dim (192: GLM shape)")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--compare-no-pdl", action="store_true", help="also time the graphs without PDL")
     ap.add_argument("--no-e2e", action="store_true")

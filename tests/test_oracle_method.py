@@ -38,10 +38,11 @@ def _layer(seed, H, M, fmt):
     return d["q_nope"], d["q_pe"], d["weight"], d["weight_scale"]
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
-def test_brute_force_triple_loop(fmt):
+@pytest.mark.parametrize("fmt,K", [("bf16", 128), ("mxfp8", 128), ("bf16", 192), ("mxfp8", 192)])
+def test_brute_force_triple_loop(fmt, K):
     H, M = 2, 3
-    qn, qp, w, s = _layer(11, H, M, fmt)
+    d = inputs.make_layer(11, H, fmt, m_max=M, nope=K)
+    qn, qp, w, s = d["q_nope"], d["q_pe"], d["weight"], d["weight_scale"]
     _, acc = oracle.mla_query(qn, qp, w, s, fmt, "bf16")
     q = _lib_bf16(qn)
     if fmt == "bf16":
