@@ -21,9 +21,13 @@
  *     library never allocates, frees or synchronises on the run path.
  *   - Supported domain (vLLM PR #174, section What: "capability-gated"
  *     H = 8/11/16 and M = 1..32): num_heads H in {8, 11, 16}, tokens
- *     1 <= M <= 32, nope dim 128 (192, the GLM dim of SparkInfer PR #75,
+ *     1 <= M <= 256, nope dim 128 (192, the GLM dim of SparkInfer PR #75,
  *     section What, through mlaqp_run_strided), latent dim 512, rope dim 64,
- *     on an sm_103 (GB300) device.
+ *     on an sm_103 (GB300) device.  M <= 32 is the decode domain of the
+ *     pages; 33..256 extends it to the multi-token-prediction and
+ *     prefill-sized steps that the pages leave to the staged BMM (vLLM PR
+ *     #174, sections Safety scope and E2E topology matrix), with a tcgen05
+ *     (TMEM-accumulator) kernel in place of the decode kernel.
  *   - Status codes are the mlaqp_status values; on any non-OK status a
  *     message is available from mlaqp_last_error() on the same thread.
  *
@@ -78,7 +82,8 @@ typedef enum {
 #define MLAQP_LATENT_DIM 512
 #define MLAQP_ROPE_DIM 64
 #define MLAQP_OUT_DIM 576
-#define MLAQP_MAX_M 32
+#define MLAQP_MAX_M 256        /* tokens per call                      */
+#define MLAQP_MAX_M_DECODE 32   /* largest M of the decode kernel       */
 
 /*
  * Capability check (SparkInfer PR #75, review of api.py `can_implement`:
@@ -114,7 +119,7 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
  *                  "E4M3 output requires one")
  *   out_row_stride elements between token rows of `out`, >= 576*H, and
  *                  out_row_stride * element size a multiple of 16 bytes
- *   M              0 returns MLAQP_OK without launching; 1..32 supported
+ *   M              0 returns MLAQP_OK without launching; 1..256 supported
  *
  * q_nope, weight, weight_scale and out must be 16-byte aligned, q_pe and
  * q_scale 4-byte aligned; the bytes written to `out` may not overlap any

@@ -19,6 +19,7 @@
 #include "mlaqp.h"
 #include "mlaqp_dispatch.h"
 #include "mlaqp_kernel.cuh"
+#include "mlaqp_kernel_large.cuh"
 
 namespace {
 
@@ -57,7 +58,8 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
-// Bit (wf*2+od)*4 + (mt-1) set once that specialisation's image is loaded.
+// Bit (wf*2+od)*4 + (mt-1) set once that decode specialisation's image is
+// loaded; bit 16 + wf*2+od for the large-M kernels.
 std::atomic<uint32_t> g_prewarmed[kMaxDevices];
 std::mutex g_prewarm_mutex;
 
@@ -209,7 +211,34 @@ const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int 
   return &table[nope_idx][out_dtype][mt - 1][trig];
 }
 
+const KernelInfo* lookup_large(int weight_format, int out_dtype, int nope_idx) {
+  return &mlaqp::kernels_large_m()[nope_idx][weight_format][out_dtype];
+}
+
+// Chunks of kLargeTokTile tokens of a large-M call (grid.z).
+int large_chunks(int M) { return (M + mlaqp::kLargeTokTile - 1) / mlaqp::kLargeTokTile; }
+
+// Dynamic shared memory of a large-M launch: the layout's size, padded when
+// needed so that the CTAs one SM can hold never ask for more than its 512
+// TMEM columns between them (a CTA of the largest chunk needs
+// tmem_cols_for(chunk) columns).
+int large_smem(const DeviceInfo& d, int base, int M) {
+  const int chunk = M < mlaqp::kLargeTokTile ? M : mlaqp::kLargeTokTile;
+  const int cols = static_cast<int>(mlaqp::tmem_cols_for((chunk + 15) & ~15));
+  const int max_ctas = 512 / cols;
+  if (d.smem_per_sm / (base + d.reserved_per_block) <= max_ctas) return base;
+  const int bytes = d.smem_per_sm / (max_ctas + 1) - d.reserved_per_block + 1;
+  return bytes < d.max_smem_optin ? bytes : d.max_smem_optin;
+}
+
 int setup_kernels(const DeviceInfo& d) {
+  for (int ki = 0; ki < 2; ++ki)
+    for (int wf = 0; wf < 2; ++wf)
+      for (int od = 0; od < 2; ++od) {
+        const cudaError_t e = cudaFuncSetAttribute(lookup_large(wf, od, ki)->fn,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
+        if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+      }
   const int smem = policy_max_smem(d);
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
@@ -268,7 +297,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   if (!valid_enums(a.weight_format, a.out_dtype)) return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format or out_dtype");
   if (M < 0) return fail(MLAQP_ERR_INVALID_ARG, "M must be >= 0");
   if (!supported_heads(H)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
-  if (M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "M must be <= 32");
+  if (M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "M must be <= 256");
   const int ki = nope_index(K);
   if (ki < 0) return fail(MLAQP_ERR_UNSUPPORTED, "nope_dim must be 128 or 192");
   if (M == 0) return MLAQP_OK;
@@ -318,9 +347,17 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  const LaunchPolicy pol = launch_policy(a.weight_format, M);
-  const KernelInfo* k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki);
-  const int smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
+  const bool large = M > MLAQP_MAX_M_DECODE;
+  const KernelInfo* k = nullptr;
+  int smem_bytes = 0;
+  if (large) {
+    k = lookup_large(a.weight_format, a.out_dtype, ki);
+    smem_bytes = large_smem(g_dev[device], k->smem_bytes, M);
+  } else {
+    const LaunchPolicy pol = launch_policy(a.weight_format, M);
+    k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki);
+    smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
+  }
   RunParams params;
   st = encode_weight_map(&params.wmap, a.weight, H, K, mx);
   if (st != MLAQP_OK) return st;
@@ -340,7 +377,8 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   params.H = H;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H),
+                     static_cast<unsigned>(large ? large_chunks(M) : 1));
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -365,7 +403,7 @@ int mlaqp_can_implement(int num_heads, int max_m, int nope_dim, int latent_dim, 
                         int out_dtype, int device) {
   if (!valid_enums(weight_format, out_dtype)) return fail(0, "unknown weight_format or out_dtype");
   if (!supported_heads(num_heads)) return fail(0, "num_heads must be 8, 11 or 16");
-  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(0, "max_m must be in 1..32");
+  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(0, "max_m must be in 1..256");
   if (nope_index(nope_dim) < 0 || latent_dim != MLAQP_LATENT_DIM || rope_dim != MLAQP_ROPE_DIM)
     return fail(0, "only nope_dim 128 or 192, latent_dim 512 and rope_dim 64 are implemented");
   int dev = 0;
@@ -381,7 +419,7 @@ int mlaqp_can_implement(int num_heads, int max_m, int nope_dim, int latent_dim, 
 int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, int device) {
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(num_heads)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
-  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "max_m must be in 1..32");
+  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "max_m must be in 1..256");
   int dev = 0;
   int st = resolve_device(device, &dev);
   if (st != MLAQP_OK) return st;
@@ -394,7 +432,8 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
   if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
   if (prev != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return fail_cuda("cudaSetDevice", e);
   int status = MLAQP_OK;
-  for (int mt = 1; mt <= (max_m + 7) / 8 && status == MLAQP_OK; ++mt) {
+  const int decode_m = max_m < MLAQP_MAX_M_DECODE ? max_m : MLAQP_MAX_M_DECODE;
+  for (int mt = 1; mt <= (decode_m + 7) / 8 && status == MLAQP_OK; ++mt) {
     const uint32_t bit = 1u << (((weight_format * 2 + out_dtype) * 4) + (mt - 1));
     if (g_prewarmed[dev].load(std::memory_order_acquire) & bit) continue;
     for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)
@@ -406,6 +445,15 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
       }
     if (status != MLAQP_OK) break;
     g_prewarmed[dev].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const uint32_t large_bit = 1u << (16 + weight_format * 2 + out_dtype);
+  if (status == MLAQP_OK && max_m > MLAQP_MAX_M_DECODE && !(g_prewarmed[dev].load(std::memory_order_acquire) & large_bit)) {
+    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki) {
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki)->fn);
+      if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
+    }
+    if (status == MLAQP_OK) g_prewarmed[dev].fetch_or(large_bit, std::memory_order_acq_rel);
   }
   if (prev != dev) cudaSetDevice(prev);
   return status;
@@ -439,6 +487,12 @@ int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q
 int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas, int* threads_per_cta) {
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
+  if (M > MLAQP_MAX_M_DECODE) {
+    const KernelInfo* k = lookup_large(weight_format, out_dtype, 0);
+    if (grid_ctas) *grid_ctas = k->tiles_per_head * H * large_chunks(M);
+    if (threads_per_cta) *threads_per_cta = k->threads;
+    return MLAQP_OK;
+  }
   const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, M).trig, 0);
   if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
   if (threads_per_cta) *threads_per_cta = k->threads;
@@ -458,11 +512,12 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
 
 int mlaqp_device_status(unsigned int* status, int reset) {
   if (!status) return fail(MLAQP_ERR_INVALID_ARG, "status must not be NULL");
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   cudaError_t e = mlaqp::device_status_bf16_weights(&a, reset != 0);
   if (e == cudaSuccess) e = mlaqp::device_status_mxfp8_weights(&b, reset != 0);
+  if (e == cudaSuccess) e = mlaqp::device_status_large_m(&c, reset != 0);
   if (e != cudaSuccess) return fail_cuda("reading the device status word", e);
-  *status = a | b;
+  *status = a | b | c;
   return MLAQP_OK;
 }
 

@@ -24,8 +24,15 @@ using KernelTable = KernelInfo[2][2][4][kTrigVariants];
 const KernelTable& kernels_bf16_weights();
 const KernelTable& kernels_mxfp8_weights();
 
+// tcgen05 kernels for 32 < M <= 256, [nope][weight_format][out_dtype]; the
+// grid is (tiles_per_head, H, ceil(M / tokens per CTA)) and smem_bytes the
+// unpadded layout size.
+using LargeKernelTable = KernelInfo[2][2][2];
+const LargeKernelTable& kernels_large_m();
+
 // Device status word of each instantiation unit (current device).
 cudaError_t device_status_bf16_weights(unsigned int* value, bool reset);
 cudaError_t device_status_mxfp8_weights(unsigned int* value, bool reset);
+cudaError_t device_status_large_m(unsigned int* value, bool reset);
 
 }  // namespace mlaqp

@@ -1,0 +1,40 @@
+// Instantiations of the tcgen05 query kernel for 33 <= M <= 256 (both weight
+// formats, both output dtypes, nope dims 128 and 192).
+#include "mlaqp_dispatch.h"
+#include "mlaqp_kernel_large.cuh"
+
+namespace mlaqp {
+namespace {
+
+template <int K, int WF, int OD>
+KernelInfo entry() {
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, kLargeTokTile>),
+                    kLargeThreads, kLargeTilesPerHead, large_smem_layout(K, kLargeTokTile).bytes};
+}
+
+template <int K>
+void fill(KernelInfo (&t)[2][2]) {
+  t[kWeightBF16][kOutBF16] = entry<K, kWeightBF16, kOutBF16>();
+  t[kWeightBF16][kOutE4M3] = entry<K, kWeightBF16, kOutE4M3>();
+  t[kWeightMXFP8][kOutBF16] = entry<K, kWeightMXFP8, kOutBF16>();
+  t[kWeightMXFP8][kOutE4M3] = entry<K, kWeightMXFP8, kOutE4M3>();
+}
+
+struct Table {
+  LargeKernelTable t;
+  Table() {
+    fill<128>(t[0]);
+    fill<192>(t[1]);
+  }
+};
+
+}  // namespace
+
+const LargeKernelTable& kernels_large_m() {
+  static const Table table;
+  return table.t;
+}
+
+cudaError_t device_status_large_m(unsigned int* value, bool reset) { return read_device_status(value, reset); }
+
+}  // namespace mlaqp

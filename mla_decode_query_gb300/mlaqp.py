@@ -36,7 +36,8 @@ NOPE_DIM = 128
 LATENT_DIM = 512
 ROPE_DIM = 64
 OUT_DIM = 576
-MAX_M = 32
+MAX_M = 256
+MAX_M_DECODE = 32
 
 WEIGHT_FORMATS = {"bf16": MLAQP_WEIGHT_BF16, "mxfp8": MLAQP_WEIGHT_MXFP8}
 OUT_DTYPES = {"bf16": MLAQP_OUT_BF16, "e4m3": MLAQP_OUT_E4M3}

@@ -47,7 +47,7 @@ def _run(**kw):
     (dict(M=-1), mq.MLAQP_ERR_INVALID_ARG),
     (dict(H=12), mq.MLAQP_ERR_UNSUPPORTED),
     (dict(H=32), mq.MLAQP_ERR_UNSUPPORTED),
-    (dict(M=33), mq.MLAQP_ERR_UNSUPPORTED),
+    (dict(M=257), mq.MLAQP_ERR_UNSUPPORTED),
     (dict(q_nope=None), mq.MLAQP_ERR_INVALID_ARG),
     (dict(q_pe=None), mq.MLAQP_ERR_INVALID_ARG),
     (dict(weight=None), mq.MLAQP_ERR_INVALID_ARG),
@@ -90,7 +90,7 @@ def test_valid_arguments_reach_the_device_check(built_library):
 
 def test_can_implement_domain(built_library):
     # Shape gating is decided before the device is queried.
-    for bad in [dict(num_heads=12), dict(max_m=0), dict(max_m=33), dict(nope_dim=192),
+    for bad in [dict(num_heads=12), dict(max_m=0), dict(max_m=257), dict(nope_dim=256),
                 dict(latent_dim=256), dict(rope_dim=32), dict(weight_format=5)]:
         a = dict(num_heads=16, max_m=32)
         a.update(bad)
@@ -103,7 +103,13 @@ def test_launch_shape(built_library):
             st, grid, threads = mq.mlaqp_launch_shape(m, h, "mxfp8", "e4m3")
             # one 4-warp token group up to M=8, two groups above
             assert st == mq.MLAQP_OK and grid == 8 * h and threads == (128 if m <= 8 else 256)
+    # above M = 32: the tcgen05 kernel, 4 CTAs of 128 threads per head and
+    # 64-token chunk
+    for m, chunks in ((33, 1), (64, 1), (65, 2), (200, 4), (256, 4)):
+        st, grid, threads = mq.mlaqp_launch_shape(m, 11, "bf16", "bf16")
+        assert st == mq.MLAQP_OK and grid == 4 * 11 * chunks and threads == 128
     assert mq.mlaqp_launch_shape(0, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
+    assert mq.mlaqp_launch_shape(257, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(4, 12)[0] == mq.MLAQP_ERR_UNSUPPORTED
 
 

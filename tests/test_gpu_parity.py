@@ -57,7 +57,7 @@ def test_can_implement_and_prewarm(cuda_device):
             for h in (8, 11, 16):
                 assert mq.mlaqp_can_implement(h, 32, weight_format=fmt, out_dtype=od) == 1, mq.mlaqp_last_error()
                 assert mq.mlaqp_prewarm(h, 32, fmt, od) == mq.MLAQP_OK, mq.mlaqp_last_error()
-    assert mq.mlaqp_can_implement(16, 33) == 0
+    assert mq.mlaqp_can_implement(16, 257) == 0
 
 
 def test_single_layer_bf16_h16_m1(cuda_device):
