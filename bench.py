@@ -61,7 +61,9 @@ class LayerSet:
         self.weight_format, self.out_dtype, self.L, self.H, self.K = weight_format, out_dtype, n_layers, h, nope
         self.m_points = tuple(m_points)
         ci = CONFIG_INDEX[weight_format] if config_index is None else config_index
-        self.host = [inputs.make_layer(inputs.layer_seed(ci, l), h, weight_format, nope=nope) for l in range(n_layers)]
+        m_max = max(32, max(self.m_points))  # the first 32 token rows do not depend on m_max
+        self.host = [inputs.make_layer(inputs.layer_seed(ci, l), h, weight_format, m_max=m_max, nope=nope)
+                     for l in range(n_layers)]
         wdt = torch.int16 if weight_format == "bf16" else torch.uint8
         w = np.stack([d["weight"] for d in self.host])
         self.weight = torch.from_numpy(w.view(np.int16) if weight_format == "bf16" else w).to(device)
@@ -268,6 +270,11 @@ WORKLOAD = ("fused MLA query projection, H=16, K=128, N=512, rope=64; BF16->BF16
             "M in {1,2,4,8,16,32}; 128 (BF16) / 256 (MXFP8) rotated layers per CUDA-graph replay")
 
 
+def workload_name(nope, m_points):
+    w = WORKLOAD.replace("M in {1,2,4,8,16,32}", "M in {" + ",".join(map(str, m_points)) + "}")
+    return w if nope == 128 else w.replace("K=128", f"K={nope}")
+
+
 def run_gpu(args):
     import torch
     import mla_decode_query_gb300 as mq
@@ -366,7 +373,9 @@ def run_gpu(args):
     if traffic_table and all((dominant, M) in traffic_table for _, M in dom_points):
         traffic = round(sum(traffic_table[(dominant, M)] * s.L for s, M in dom_points) /
                         sum(s.L for s, _ in dom_points))
-    roof = {"bound": "hbm", "kernel": f"mlaqp_fused_query_kernel ({dominant})",
+    kernel_names = sorted({"mlaqp_fused_query_large_kernel" if M > 32 else "mlaqp_fused_query_kernel"
+                           for _, M in dom_points})
+    roof = {"bound": "hbm", "kernel": f"{' + '.join(kernel_names)} ({dominant})",
             "achieved": round(ach, 1), "peak": peaks[0], "unit": "GB/s",
             "frac": round(ach / peaks[0], 4), "peak_source": peaks[1], "traffic": traffic,
             "traffic_source": TRAFFIC_FILE if traffic else "kernel changed since the last ncu capture",
@@ -378,7 +387,7 @@ def run_gpu(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD if args.nope == 128 else WORKLOAD.replace("K=128", f"K={args.nope}"),
+            "config": {"workload": workload_name(args.nope, m_points),
                        "heads": H, "nope_dim": args.nope, "m_points": list(m_points),
                        "layers": {s.weight_format: s.L for s in sets}, "pdl": not args.no_pdl,
                        "l2": f"rotated weights per replay {[s.L * s.bytes_per_call(1) >> 20 for s in sets]} MiB "
