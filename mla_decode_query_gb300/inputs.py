@@ -102,3 +102,45 @@ def small_integer_layer(seed: int, H: int, M: int, weight_format: str, nope: int
         scale = np.full((H, nope, LATENT // 32), 127, dtype=np.uint8)
     return {"q_nope": _to_bf16_bits(q), "q_pe": _to_bf16_bits(pe), "weight": weight,
             "weight_scale": scale}
+
+
+V_HEAD = 128
+
+
+def make_v_layer(seed: int, H: int, weight_format: str, m_max: int = M_MAX) -> dict:
+    """Draw one layer's V up-projection inputs (same recipe style):
+
+    1. ``W_UV[h,c,d]`` ~ N(0, 1/sqrt(512)), ``[H,512,128]``, cast to BF16 or E4M3;
+    2. MXFP8 only: E8M0 bytes ``127 + U{-4..2}``, ``[H,512,4]`` (one per 32
+       consecutive output elements of each (h,c) row);
+    3. ``x`` (attention output in the latent space) ~ N(0,1), ``[m_max,H,512]``,
+       cast to BF16.
+    Returns ``x`` uint16, ``weight`` uint16 / uint8, ``weight_scale`` uint8 or None.
+    """
+    if weight_format not in ("bf16", "mxfp8"):
+        raise ValueError(f"unknown weight format {weight_format!r}")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    w = rng.standard_normal((H, LATENT, V_HEAD), dtype=np.float32) * np.float32(1.0 / np.sqrt(LATENT))
+    if weight_format == "bf16":
+        weight, scale = _to_bf16_bits(w), None
+    else:
+        weight = _to_e4m3_bits(w)
+        scale = (127 + rng.integers(-4, 3, size=(H, LATENT, V_HEAD // 32))).astype(np.uint8)
+    x = _to_bf16_bits(rng.standard_normal((m_max, H, LATENT), dtype=np.float32))
+    return {"x": x, "weight": weight, "weight_scale": scale}
+
+
+def small_integer_v_layer(seed: int, H: int, M: int, weight_format: str) -> dict:
+    """V up-projection inputs whose sums are exact in binary32: ``x`` in
+    {-2..2}, weights in {-1, 0, 1} (scale byte 127), every partial sum an
+    integer of magnitude <= 1024, so any summation order gives the same FP32
+    value and the same BF16 rounding."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    x = rng.integers(-2, 3, size=(M, H, LATENT)).astype(np.float32)
+    w = rng.integers(-1, 2, size=(H, LATENT, V_HEAD)).astype(np.float32)
+    if weight_format == "bf16":
+        weight, scale = _to_bf16_bits(w), None
+    else:
+        weight = _to_e4m3_bits(w)
+        scale = np.full((H, LATENT, V_HEAD // 32), 127, dtype=np.uint8)
+    return {"x": _to_bf16_bits(x), "weight": weight, "weight_scale": scale}

@@ -9,6 +9,7 @@ from .mlaqp_oracle import (  # noqa: F401
     LATENT_DIM,
     MX_BLOCK,
     NOPE_DIM,
+    V_HEAD_DIM,
     OUT_DIM,
     ROPE_DIM,
     algorithmic_bytes,
@@ -22,6 +23,8 @@ from .mlaqp_oracle import (  # noqa: F401
     f32_to_e4m3_satfinite,
     f64_to_bf16_rne,
     mla_query,
+    mla_v_up,
     project,
+    v_up_algorithmic_bytes,
     write_workspace,
 )

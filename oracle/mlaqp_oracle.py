@@ -35,6 +35,14 @@ Readings of the pages taken here (the pages are silent or garbled):
   otherwise round-to-nearest-even including subnormals; the division by
   ``q_scale`` is an IEEE float32 division of the BF16-rounded value.
 
+The V up-projection after attention (``mla_v_up``): the pages name it only
+as the downstream step that a separate change handles (vLLM PR #174, section
+Safety scope).  Reading taken: per head, the attention output over the latent
+cache ``x[M,H,512]`` (BF16) times ``W_UV[H,512,128]``, FP32 accumulation,
+BF16 output ``[M,H,128]``; ``W_UV`` is stored with its output (v) axis
+fastest, BF16 or MXFP8 with one E8M0 scale per 32 consecutive output
+elements of each (h,c) row (``[H,512,4]``), the convention of ``W_UK_T``.
+
 Functions whose behaviour is pinned only by the format specifications and
 closed forms (no worked example is printed on the pages): all of them.  The
 pins live in ``tests/test_oracle_*.py``.
@@ -46,6 +54,7 @@ import numpy as np
 
 NOPE_DIM = 128
 LATENT_DIM = 512
+V_HEAD_DIM = 128
 ROPE_DIM = 64
 OUT_DIM = LATENT_DIM + ROPE_DIM
 MX_BLOCK = 32
@@ -173,7 +182,8 @@ def e8m0_to_f64(codes) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def decode_weight(weight, weight_scale, weight_format: str) -> np.ndarray:
-    """Return W_UK_T as float64 ``[H,K,N]``.
+    """Return a per-head weight (W_UK_T ``[H,K,N]``, or W_UV ``[H,512,128]``
+    with K the contraction and N the output axis) as float64.
 
     ``weight_format == "bf16"``: ``weight`` holds BF16 bits ``[H,K,N]``.
     ``weight_format == "mxfp8"``: ``weight`` holds E4M3 codes ``[H,K,N]`` and
@@ -286,3 +296,32 @@ def algorithmic_bytes(M: int, H: int, weight_format: str, out_dtype: str,
     w = H * nope * latent * wb
     s = H * nope * (latent // MX_BLOCK) if weight_format == "mxfp8" else 0
     return w + s + 2 * M * H * nope + 2 * M * H * rope + M * H * (latent + rope) * ob
+
+
+# ---------------------------------------------------------------------------
+# The V up-projection (the step after attention over the latent cache)
+# ---------------------------------------------------------------------------
+
+def mla_v_up(x, weight, weight_scale, weight_format: str):
+    """V up-projection of one layer call.
+
+    ``x``: BF16 bits ``[M,H,512]`` (attention output in the latent space);
+    ``weight``: W_UV, BF16 bits or E4M3 codes ``[H,512,128]``;
+    ``weight_scale``: E8M0 ``[H,512,4]`` (MXFP8) or None.
+    out[m,h,d] = bf16_rne(sum_c x[m,h,c] * W_UV[h,c,d]).
+    Returns ``(out, acc)``: uint16 bits ``[M,H,128]`` and the float64 sums.
+    """
+    w64 = decode_weight(weight, weight_scale, weight_format)
+    if w64.shape[1:] != (LATENT_DIM, V_HEAD_DIM):
+        raise ValueError("W_UV must be [H,512,128]")
+    acc = project(x, w64)
+    return f64_to_bf16_rne(acc), acc
+
+
+def v_up_algorithmic_bytes(M: int, H: int, weight_format: str, latent: int = LATENT_DIM,
+                           v_dim: int = V_HEAD_DIM) -> int:
+    """Bytes one V up-projection call must move at least once: W_UV (+ scales),
+    the attention output x and the BF16 result."""
+    wb = 2 if weight_format == "bf16" else 1
+    s = H * latent * (v_dim // MX_BLOCK) if weight_format == "mxfp8" else 0
+    return H * latent * v_dim * wb + s + 2 * M * H * latent + 2 * M * H * v_dim

@@ -50,3 +50,23 @@ def test_small_integer_layer_values():
     assert set(np.unique(q)) <= {-2.0, -1.0, 0.0, 1.0, 2.0}
     w = _f(d["weight"])
     assert set(np.unique(w)) <= {-1.0, 0.0, 1.0}
+
+
+def test_v_layer_shapes_and_determinism():
+    from mla_decode_query_gb300 import inputs as inp
+    for fmt in ("bf16", "mxfp8"):
+        a = inp.make_v_layer(5, 11, fmt, m_max=7)
+        b = inp.make_v_layer(5, 11, fmt, m_max=7)
+        assert a["x"].shape == (7, 11, 512) and a["x"].dtype == np.uint16
+        assert a["weight"].shape == (11, 512, 128)
+        assert a["weight"].dtype == (np.uint16 if fmt == "bf16" else np.uint8)
+        for k in ("x", "weight"):
+            np.testing.assert_array_equal(a[k], b[k])
+        if fmt == "mxfp8":
+            s = a["weight_scale"]
+            assert s.shape == (11, 512, 4) and s.min() >= 123 and s.max() <= 129
+        else:
+            assert a["weight_scale"] is None
+    w = inp.make_v_layer(6, 16, "bf16")["weight"]
+    wf = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert abs(wf.std() * np.sqrt(512) - 1) < 0.02
