@@ -208,6 +208,57 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
  */
 int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t stream);
 
+/*
+ * V up-projection, the step after attention over the latent cache (the
+ * pages name it only as the downstream V up-projection, vLLM PR #174,
+ * section Safety scope; the weight formats follow the query side, section
+ * What).  For every token m < M and head h < H:
+ *
+ *   out[m,h,d] = bf16_rne( sum_{c<512} x[m,h,c] * W_UV[h,c,d] )   d < 128, FP32 accumulation
+ *
+ * in one kernel launch on `stream`, asynchronous, no allocation, no host
+ * synchronisation.
+ *   x              BF16 attention output in the latent space; element (m,h,c)
+ *                  at x[m*x_token_stride + h*x_head_stride + c], c < 512;
+ *                  strides in elements, >= 0, multiples of 8; 16-byte aligned
+ *   weight         W_UV [H, 512, 128], output (d) axis fastest: BF16
+ *                  (MLAQP_WEIGHT_BF16) or OCP E4M3FN codes (MLAQP_WEIGHT_MXFP8);
+ *                  16-byte aligned
+ *   weight_scale   E8M0 [H, 512, 4] for MXFP8 (byte j of row (h,c) scales
+ *                  d in [32j, 32j+32) by 2^(x-127)), NULL for BF16
+ *   out            BF16; element (m,h,d) at out[m*out_row_stride + h*128 + d];
+ *                  out_row_stride >= 128*H and a multiple of 8 elements;
+ *                  16-byte aligned; rows >= M and the padding are not written;
+ *                  may not overlap an input
+ *   M              0 returns MLAQP_OK without launching; 1..32 supported
+ *   H              8, 11 or 16
+ *   pdl            != 0: programmatic dependent launch, as mlaqp_run_pdl (the
+ *                  weights and scales must not be written by the kernel
+ *                  launched just before on `stream`)
+ * Status codes as for mlaqp_run.
+ */
+#define MLAQP_V_HEAD_DIM 128
+int mlaqp_v_up_run(const void* x, int64_t x_token_stride, int64_t x_head_stride, const void* weight,
+                   const void* weight_scale, void* out, int64_t out_row_stride, int M, int H,
+                   int weight_format, int pdl, mlaqp_stream_t stream);
+
+/* 1 if mlaqp_v_up_run covers (num_heads, max_m, weight_format) on `device`
+ * (< 0: current), else 0 with a reason in mlaqp_last_error().  Launches
+ * nothing. */
+int mlaqp_v_up_can_implement(int num_heads, int max_m, int weight_format, int device);
+
+/* Loads every V up-projection kernel a call with M <= max_m can use, as
+ * mlaqp_prewarm does for the query projection.  Call before graph capture. */
+int mlaqp_v_up_prewarm(int num_heads, int max_m, int weight_format, int device);
+
+/* Test hook for the V up-projection's bounded waits, as
+ * mlaqp_debug_run_bounded_wait (no counterpart on the pages). */
+int mlaqp_debug_v_up_bounded_wait(const void* x, int64_t x_token_stride, int64_t x_head_stride,
+                                  const void* weight, const void* weight_scale, void* out,
+                                  int64_t out_row_stride, int M, int H, int weight_format,
+                                  unsigned long long wait_limit_ns, unsigned int extra_tx_bytes,
+                                  mlaqp_stream_t stream);
+
 /* Message of the last non-OK status returned on this thread ("" if none). */
 const char* mlaqp_last_error(void);
 

@@ -1,4 +1,5 @@
-"""GB300-native fused MLA decode query projection and assembly.
+"""GB300-native fused MLA decode query projection and assembly (and the V
+up-projection after attention).
 
 The operation runs in ``libmlaqp.so`` (CUDA C++ for sm_103a, C ABI in
 ``include/mlaqp.h``); ``mla_decode_query_gb300.mlaqp`` is its thin ctypes
@@ -9,6 +10,8 @@ fails loudly if it has not been built.
 
 from .mlaqp import (  # noqa: F401
     MAX_M,
+    MAX_M_DECODE,
+    V_HEAD_DIM,
     MLAQP_DEVSTATUS_WAIT_TIMEOUT,
     MLAQP_ERR_CUDA,
     MLAQP_ERR_INVALID_ARG,
@@ -25,6 +28,7 @@ from .mlaqp import (  # noqa: F401
     mlaqp_can_implement,
     mlaqp_debug_launch_null,
     mlaqp_debug_run_bounded_wait,
+    mlaqp_debug_v_up_bounded_wait,
     mlaqp_device_status,
     mlaqp_last_error,
     mlaqp_launch_shape,
@@ -32,6 +36,9 @@ from .mlaqp import (  # noqa: F401
     mlaqp_run,
     mlaqp_run_pdl,
     mlaqp_run_strided,
+    mlaqp_v_up_can_implement,
+    mlaqp_v_up_prewarm,
+    mlaqp_v_up_run,
     mlaqp_version,
 )
 

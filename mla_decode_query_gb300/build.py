@@ -24,7 +24,8 @@ BUILD_DIR = PKG_DIR / "_build"
 LIB_DIR = PKG_DIR / "_lib"
 LIB_PATH = LIB_DIR / "libmlaqp.so"
 
-SOURCES = ["mlaqp_api.cu", "mlaqp_kernels_bf16.cu", "mlaqp_kernels_mxfp8.cu", "mlaqp_kernels_large.cu"]
+SOURCES = ["mlaqp_api.cu", "mlaqp_kernels_bf16.cu", "mlaqp_kernels_mxfp8.cu", "mlaqp_kernels_large.cu",
+           "mlaqp_kernels_v_up.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -20,6 +20,7 @@
 #include "mlaqp_dispatch.h"
 #include "mlaqp_kernel.cuh"
 #include "mlaqp_kernel_large.cuh"
+#include "mlaqp_v_up_kernel.cuh"
 
 namespace {
 
@@ -232,6 +233,14 @@ int large_smem(const DeviceInfo& d, int base, int M) {
 }
 
 int setup_kernels(const DeviceInfo& d) {
+  for (int wf = 0; wf < 2; ++wf)
+    for (int mt = 0; mt < 4; ++mt)
+      for (int trig = 0; trig < 2; ++trig) {
+        const KernelInfo& k = mlaqp::kernels_v_up()[wf][mt][trig];
+        const cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   smem_for_cap(d, k.smem_bytes, 3));
+        if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+      }
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
       for (int od = 0; od < 2; ++od) {
@@ -395,6 +404,117 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   return MLAQP_OK;
 }
 
+// ---------------------------------------------------------------------------
+// V up-projection
+// ---------------------------------------------------------------------------
+
+// 2-D tensor map over W_UV viewed as [H*512 rows][128 columns]; one box is
+// 16 columns x 256 rows (a CTA copies two), unswizzled.
+int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
+  std::string err;
+  EncodeTiledFn fn = encode_tiled_fn(&err);
+  if (!fn) return fail(MLAQP_ERR_CUDA, err);
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLAQP_V_HEAD_DIM),
+                              static_cast<cuuint64_t>(H) * MLAQP_LATENT_DIM};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(MLAQP_V_HEAD_DIM) * (mx ? 1 : 2)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(mlaqp::kVNTile), 256};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(weight), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MLAQP_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return MLAQP_OK;
+}
+
+const KernelInfo* lookup_v_up(int weight_format, int M, int trig) {
+  return &mlaqp::kernels_v_up()[weight_format][(M + 7) / 8 - 1][trig];
+}
+
+struct VUpArgs {
+  const void* x;
+  int64_t x_ts, x_hs;
+  const void* weight;
+  const void* weight_scale;
+  void* out;
+  int64_t out_row_stride;
+  int M, H, weight_format;
+};
+
+int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
+  const int M = a.M, H = a.H;
+  if (a.weight_format != MLAQP_WEIGHT_BF16 && a.weight_format != MLAQP_WEIGHT_MXFP8)
+    return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format");
+  if (M < 0) return fail(MLAQP_ERR_INVALID_ARG, "M must be >= 0");
+  if (!supported_heads(H)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
+  if (M > MLAQP_MAX_M_DECODE) return fail(MLAQP_ERR_UNSUPPORTED, "M must be <= 32 for the V up-projection");
+  if (M == 0) return MLAQP_OK;
+  const bool mx = a.weight_format == MLAQP_WEIGHT_MXFP8;
+  if (!a.x || !a.weight || !a.out) return fail(MLAQP_ERR_INVALID_ARG, "x, weight and out are required");
+  if (mx && !a.weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "MXFP8 weights require weight_scale");
+  if (!mx && a.weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 weights take no weight_scale (pass NULL)");
+  if (!aligned(a.x, 16) || !aligned(a.weight, 16) || !aligned(a.out, 16) ||
+      (a.weight_scale && !aligned(a.weight_scale, 16)))
+    return fail(MLAQP_ERR_INVALID_ARG, "x, weight, weight_scale and out must be 16-byte aligned");
+  if (a.x_ts < 0 || a.x_hs < 0 || a.x_ts % 8 != 0 || a.x_hs % 8 != 0)
+    return fail(MLAQP_ERR_INVALID_ARG, "x strides must be >= 0 and multiples of 8 elements (16 bytes)");
+  if (a.out_row_stride < static_cast<int64_t>(MLAQP_V_HEAD_DIM) * H)
+    return fail(MLAQP_ERR_INVALID_ARG, "out_row_stride must be >= 128*H elements");
+  if (a.out_row_stride % 8 != 0) return fail(MLAQP_ERR_INVALID_ARG, "out_row_stride must be a multiple of 8 elements");
+
+  const Range o = span(a.out, static_cast<size_t>(((M - 1) * a.out_row_stride + MLAQP_V_HEAD_DIM * H) * 2));
+  const size_t w_elems = static_cast<size_t>(H) * MLAQP_LATENT_DIM * MLAQP_V_HEAD_DIM;
+  const Range inputs[3] = {
+      span(a.x, static_cast<size_t>((M - 1) * a.x_ts + (H - 1) * a.x_hs + MLAQP_LATENT_DIM) * 2),
+      span(a.weight, w_elems * (mx ? 1 : 2)),
+      span(a.weight_scale, mx ? w_elems / 32 : 0),
+  };
+  for (const Range& r : inputs)
+    if (r.hi > r.lo && overlaps(o, r)) return fail(MLAQP_ERR_INVALID_ARG, "out overlaps an input tensor");
+
+  int device = 0;
+  int st = resolve_device(-1, &device);
+  if (st != MLAQP_OK) return st;
+  st = check_device(device);
+  if (st != MLAQP_OK) return st;
+
+  // Same trigger / CTA-cap policy as the query kernel (same CTA count per
+  // head, similar per-CTA weight tile).
+  const LaunchPolicy pol = launch_policy(a.weight_format, M);
+  const KernelInfo* k = lookup_v_up(a.weight_format, M, pol.trig == 0 ? 0 : 1);
+  const int smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
+  mlaqp::VUpParams params;
+  st = encode_v_weight_map(&params.wmap, a.weight, H, mx);
+  if (st != MLAQP_OK) return st;
+  params.x = static_cast<const uint16_t*>(a.x);
+  params.x_ts = a.x_ts;
+  params.x_hs = a.x_hs;
+  params.weight_scale = static_cast<const uint8_t*>(a.weight_scale);
+  params.out = static_cast<uint16_t*>(a.out);
+  params.out_row_stride = a.out_row_stride;
+  params.wait_limit_ns = wait_limit_ns;
+  params.extra_tx = extra_tx;
+  params.M = M;
+  params.H = H;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H), 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {&params};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, k->fn, args);
+  if (e != cudaSuccess) return fail_cuda("cudaLaunchKernelExC", e);
+  return MLAQP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -512,12 +632,13 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
 
 int mlaqp_device_status(unsigned int* status, int reset) {
   if (!status) return fail(MLAQP_ERR_INVALID_ARG, "status must not be NULL");
-  unsigned int a = 0, b = 0, c = 0;
+  unsigned int a = 0, b = 0, c = 0, v = 0;
   cudaError_t e = mlaqp::device_status_bf16_weights(&a, reset != 0);
   if (e == cudaSuccess) e = mlaqp::device_status_mxfp8_weights(&b, reset != 0);
   if (e == cudaSuccess) e = mlaqp::device_status_large_m(&c, reset != 0);
+  if (e == cudaSuccess) e = mlaqp::device_status_v_up(&v, reset != 0);
   if (e != cudaSuccess) return fail_cuda("reading the device status word", e);
-  *status = a | b | c;
+  *status = a | b | c | v;
   return MLAQP_OK;
 }
 
@@ -539,6 +660,64 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
   const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&mlaqp_null_kernel), args);
   if (e != cudaSuccess) return fail_cuda("cudaLaunchKernelExC", e);
   return MLAQP_OK;
+}
+
+int mlaqp_v_up_run(const void* x, int64_t x_token_stride, int64_t x_head_stride, const void* weight,
+                   const void* weight_scale, void* out, int64_t out_row_stride, int M, int H, int weight_format,
+                   int pdl, mlaqp_stream_t stream) {
+  const VUpArgs a{x, x_token_stride, x_head_stride, weight, weight_scale, out, out_row_stride, M, H, weight_format};
+  return v_up_impl(a, stream, pdl != 0, kDefaultWaitLimitNs, 0);
+}
+
+int mlaqp_debug_v_up_bounded_wait(const void* x, int64_t x_token_stride, int64_t x_head_stride, const void* weight,
+                                  const void* weight_scale, void* out, int64_t out_row_stride, int M, int H,
+                                  int weight_format, unsigned long long wait_limit_ns, unsigned int extra_tx_bytes,
+                                  mlaqp_stream_t stream) {
+  if (wait_limit_ns == 0) return fail(MLAQP_ERR_INVALID_ARG, "wait_limit_ns must be > 0");
+  if (extra_tx_bytes > (1u << 19)) return fail(MLAQP_ERR_INVALID_ARG, "extra_tx_bytes must be <= 2^19");
+  const VUpArgs a{x, x_token_stride, x_head_stride, weight, weight_scale, out, out_row_stride, M, H, weight_format};
+  return v_up_impl(a, stream, false, wait_limit_ns, extra_tx_bytes);
+}
+
+int mlaqp_v_up_can_implement(int num_heads, int max_m, int weight_format, int device) {
+  if (weight_format != MLAQP_WEIGHT_BF16 && weight_format != MLAQP_WEIGHT_MXFP8)
+    return fail(0, "unknown weight_format");
+  if (!supported_heads(num_heads)) return fail(0, "num_heads must be 8, 11 or 16");
+  if (max_m < 1 || max_m > MLAQP_MAX_M_DECODE) return fail(0, "max_m must be in 1..32");
+  int dev = 0;
+  if (resolve_device(device, &dev) != MLAQP_OK) return 0;
+  int count = 0;
+  const cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return fail(0, std::string("no CUDA device: ") + cudaGetErrorString(e));
+  if (dev >= count) return fail(0, "device ordinal out of range");
+  if (check_device(dev) != MLAQP_OK) return 0;
+  return 1;
+}
+
+int mlaqp_v_up_prewarm(int num_heads, int max_m, int weight_format, int device) {
+  if (weight_format != MLAQP_WEIGHT_BF16 && weight_format != MLAQP_WEIGHT_MXFP8)
+    return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format");
+  if (!supported_heads(num_heads)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
+  if (max_m < 1 || max_m > MLAQP_MAX_M_DECODE) return fail(MLAQP_ERR_UNSUPPORTED, "max_m must be in 1..32");
+  int dev = 0;
+  int st = resolve_device(device, &dev);
+  if (st != MLAQP_OK) return st;
+  st = check_device(dev);
+  if (st != MLAQP_OK) return st;
+  std::lock_guard<std::mutex> lock(g_prewarm_mutex);
+  int prev = -1;
+  cudaError_t e = cudaGetDevice(&prev);
+  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  if (prev != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return fail_cuda("cudaSetDevice", e);
+  int status = MLAQP_OK;
+  for (int mt = 1; mt <= (max_m + 7) / 8 && status == MLAQP_OK; ++mt)
+    for (int trig = 0; trig < 2 && status == MLAQP_OK; ++trig) {
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, lookup_v_up(weight_format, 8 * mt, trig)->fn);
+      if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
+    }
+  if (prev != dev) cudaSetDevice(prev);
+  return status;
 }
 
 const char* mlaqp_last_error(void) { return g_last_error.c_str(); }

@@ -30,9 +30,15 @@ const KernelTable& kernels_mxfp8_weights();
 using LargeKernelTable = KernelInfo[2][2][2];
 const LargeKernelTable& kernels_large_m();
 
+// V up-projection kernels, [weight_format][mt-1][trig] (trig 0: at entry,
+// 1: after the dependency wait); grid (tiles_per_head, H).
+using VUpKernelTable = KernelInfo[2][4][2];
+const VUpKernelTable& kernels_v_up();
+
 // Device status word of each instantiation unit (current device).
 cudaError_t device_status_bf16_weights(unsigned int* value, bool reset);
 cudaError_t device_status_mxfp8_weights(unsigned int* value, bool reset);
 cudaError_t device_status_large_m(unsigned int* value, bool reset);
+cudaError_t device_status_v_up(unsigned int* value, bool reset);
 
 }  // namespace mlaqp

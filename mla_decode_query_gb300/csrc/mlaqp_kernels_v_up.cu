@@ -1,0 +1,44 @@
+// Instantiations of the V up-projection kernel: {BF16, MXFP8} W_UV x
+// ceil(M/8) in 1..4 x trigger point {entry, after the wait}.
+#include "mlaqp_dispatch.h"
+#include "mlaqp_v_up_kernel.cuh"
+
+namespace mlaqp {
+namespace {
+
+template <int WF, int MT, int TRIG>
+KernelInfo entry() {
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_v_up_kernel<WF, MT, TRIG>), kVThreads, kVTilesPerHead,
+                    VSmem<MT>::Bytes};
+}
+
+template <int WF>
+void fill(KernelInfo (&t)[4][2]) {
+  t[0][0] = entry<WF, 1, 0>();
+  t[0][1] = entry<WF, 1, 1>();
+  t[1][0] = entry<WF, 2, 0>();
+  t[1][1] = entry<WF, 2, 1>();
+  t[2][0] = entry<WF, 3, 0>();
+  t[2][1] = entry<WF, 3, 1>();
+  t[3][0] = entry<WF, 4, 0>();
+  t[3][1] = entry<WF, 4, 1>();
+}
+
+struct Table {
+  VUpKernelTable t;
+  Table() {
+    fill<kWeightBF16>(t[kWeightBF16]);
+    fill<kWeightMXFP8>(t[kWeightMXFP8]);
+  }
+};
+
+}  // namespace
+
+const VUpKernelTable& kernels_v_up() {
+  static const Table table;
+  return table.t;
+}
+
+cudaError_t device_status_v_up(unsigned int* value, bool reset) { return read_device_status(value, reset); }
+
+}  // namespace mlaqp

@@ -38,6 +38,7 @@ ROPE_DIM = 64
 OUT_DIM = 576
 MAX_M = 256
 MAX_M_DECODE = 32
+V_HEAD_DIM = 128
 
 WEIGHT_FORMATS = {"bf16": MLAQP_WEIGHT_BF16, "mxfp8": MLAQP_WEIGHT_MXFP8}
 OUT_DTYPES = {"bf16": MLAQP_OUT_BF16, "e4m3": MLAQP_OUT_E4M3}
@@ -64,6 +65,13 @@ _SIGNATURES = {
                                               ctypes.c_int64, _c_void_p, _c_int, _c_int, _c_int, _c_int,
                                               ctypes.c_ulonglong, ctypes.c_uint, _c_void_p]),
     "mlaqp_debug_launch_null": (_c_int, [_c_int, _c_int, _c_int, _c_void_p]),
+    "mlaqp_v_up_run": (_c_int, [_c_void_p, ctypes.c_int64, ctypes.c_int64, _c_void_p, _c_void_p, _c_void_p,
+                                ctypes.c_int64, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
+    "mlaqp_v_up_can_implement": (_c_int, [_c_int] * 4),
+    "mlaqp_v_up_prewarm": (_c_int, [_c_int] * 4),
+    "mlaqp_debug_v_up_bounded_wait": (_c_int, [_c_void_p, ctypes.c_int64, ctypes.c_int64, _c_void_p, _c_void_p,
+                                               _c_void_p, ctypes.c_int64, _c_int, _c_int, _c_int,
+                                               ctypes.c_ulonglong, ctypes.c_uint, _c_void_p]),
     "mlaqp_last_error": (ctypes.c_char_p, []),
     "mlaqp_version": (_c_int, []),
 }
@@ -175,6 +183,29 @@ def mlaqp_debug_run_bounded_wait(q_nope, q_pe, weight, weight_scale, out, out_ro
 
 def mlaqp_debug_launch_null(ctas, threads, pdl, stream=None) -> int:
     return load_library().mlaqp_debug_launch_null(int(ctas), int(threads), 1 if pdl else 0, _stream(stream))
+
+
+def mlaqp_v_up_run(x, x_token_stride, x_head_stride, weight, weight_scale, out, out_row_stride, M, H,
+                   weight_format, pdl=False, stream=None) -> int:
+    return load_library().mlaqp_v_up_run(_ptr(x), int(x_token_stride), int(x_head_stride), _ptr(weight),
+                                         _ptr(weight_scale), _ptr(out), int(out_row_stride), int(M), int(H),
+                                         _fmt(weight_format, WEIGHT_FORMATS), 1 if pdl else 0, _stream(stream))
+
+
+def mlaqp_v_up_can_implement(num_heads, max_m, weight_format="bf16", device=-1) -> int:
+    return load_library().mlaqp_v_up_can_implement(num_heads, max_m, _fmt(weight_format, WEIGHT_FORMATS), device)
+
+
+def mlaqp_v_up_prewarm(num_heads, max_m, weight_format="bf16", device=-1) -> int:
+    return load_library().mlaqp_v_up_prewarm(num_heads, max_m, _fmt(weight_format, WEIGHT_FORMATS), device)
+
+
+def mlaqp_debug_v_up_bounded_wait(x, x_token_stride, x_head_stride, weight, weight_scale, out, out_row_stride, M,
+                                  H, weight_format, wait_limit_ns, extra_tx_bytes, stream=None) -> int:
+    return load_library().mlaqp_debug_v_up_bounded_wait(
+        _ptr(x), int(x_token_stride), int(x_head_stride), _ptr(weight), _ptr(weight_scale), _ptr(out),
+        int(out_row_stride), int(M), int(H), _fmt(weight_format, WEIGHT_FORMATS), int(wait_limit_ns),
+        int(extra_tx_bytes), _stream(stream))
 
 
 def mlaqp_launch_shape(M, H, weight_format="bf16", out_dtype="bf16"):

@@ -154,3 +154,42 @@ def test_strided_accepts_views_and_nope192_shapes(built_library):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; covered by the GPU tests")
     assert st == mq.MLAQP_ERR_CUDA
+
+
+def _v_up(**kw):
+    a = dict(x=A, x_token_stride=H * 512, x_head_stride=512, weight=4 * A, weight_scale=None, out=16 * A,
+             out_row_stride=128 * H, M=M, H=H, weight_format="bf16", pdl=False, stream=0)
+    a.update(kw)
+    return mq.mlaqp_v_up_run(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(weight_format=3), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(M=-1), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(H=12), mq.MLAQP_ERR_UNSUPPORTED),
+    (dict(M=33), mq.MLAQP_ERR_UNSUPPORTED),                              # V up-projection: M <= 32
+    (dict(x=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(weight=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(out=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(weight_scale=8 * A), mq.MLAQP_ERR_INVALID_ARG),                # BF16 takes no scale
+    (dict(weight_format="mxfp8"), mq.MLAQP_ERR_INVALID_ARG),             # MXFP8 needs one
+    (dict(x=A + 8), mq.MLAQP_ERR_INVALID_ARG),                           # misaligned
+    (dict(out=16 * A + 4), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(x_head_stride=516), mq.MLAQP_ERR_INVALID_ARG),                 # not a 16-byte row
+    (dict(x_token_stride=-512), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(out_row_stride=128 * H - 8), mq.MLAQP_ERR_INVALID_ARG),        # < 128*H
+    (dict(out_row_stride=128 * H + 4), mq.MLAQP_ERR_INVALID_ARG),        # 8 bytes, not 16
+    (dict(out=A + 4096), mq.MLAQP_ERR_INVALID_ARG),                      # overlaps x
+    (dict(out=4 * A + 1024), mq.MLAQP_ERR_INVALID_ARG),                  # overlaps the weights
+])
+def test_v_up_validation(built_library, kw, code):
+    assert _v_up(**kw) == code
+    assert mq.mlaqp_last_error() != ""
+
+
+def test_v_up_zero_tokens_and_domain(built_library):
+    assert _v_up(M=0, x=None, out=None) == mq.MLAQP_OK
+    for bad in [dict(num_heads=12), dict(max_m=0), dict(max_m=33), dict(weight_format=4)]:
+        a = dict(num_heads=16, max_m=32, weight_format="bf16")
+        a.update(bad)
+        assert mq.mlaqp_v_up_can_implement(**a) == 0, bad
