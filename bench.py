@@ -14,6 +14,10 @@ layers run in a decode step.
 Metric: achieved HBM GB/s = algorithmic bytes (weights + scales + q_nope +
 q_pe + output, per layer call) / time, and microseconds per layer call.
 
+--op v_up measures the V up-projection after attention instead
+(out[m,h,:128] = x[m,h,:512] @ W_UV[h], BF16 or MXFP8 W_UV, BF16 output),
+same layer rotation, same metric on its own bytes (W_UV + scales + x + out).
+
 --impl reference times the float64 CPU oracle on a bounded sample of the
 same workload on the host cores (the only other code path this file runs).
 """
@@ -36,8 +40,16 @@ M_POINTS = (1, 2, 4, 8, 16, 32)
 FORMATS = (("bf16", "bf16"), ("mxfp8", "e4m3"))
 DEFAULT_LAYERS = {"bf16": 128, "mxfp8": 256}
 CONFIG_INDEX = {"bf16": 1, "mxfp8": 3}  # seed family 1000*i + layer
+V_CONFIG_INDEX = {"bf16": 6, "mxfp8": 7}
+V_FORMATS = (("bf16", "bf16"), ("mxfp8", "bf16"))
 Q_SCALE_SEED = 3
 L2_BYTES = 126 * 2**20
+
+
+def v_up_algorithmic_bytes(M, weight_format, h=H, latent=512, v_dim=128):
+    wb = 2 if weight_format == "bf16" else 1
+    scales = h * latent * (v_dim // 32) if weight_format == "mxfp8" else 0
+    return h * latent * v_dim * wb + scales + 2 * M * h * latent + 2 * M * h * v_dim
 
 
 def algorithmic_bytes(M, weight_format, out_dtype, h=H, nope=128):
@@ -85,6 +97,15 @@ class LayerSet:
             self.q_pe[M] = self.q_pe_host[M].to(device)
             self.out[M] = torch.zeros((n_layers, M, h, 576), dtype=odt, device=device)
 
+    def host_inputs(self, M):
+        return [self.q_nope_host[M], self.q_pe_host[M]]
+
+    def dev_inputs(self, M):
+        return [self.q_nope[M], self.q_pe[M]]
+
+    def kernel_name(self, M):
+        return "mlaqp_fused_query_large_kernel" if M > 32 else "mlaqp_fused_query_kernel"
+
     def layer_args(self, M, l):
         return dict(q_nope=self.q_nope[M][l], q_pe=self.q_pe[M][l], weight=self.weight[l],
                     weight_scale=None if self.scale is None else self.scale[l], out=self.out[M][l],
@@ -122,6 +143,66 @@ class LayerSet:
 
     def bytes_per_call(self, M):
         return algorithmic_bytes(M, self.weight_format, self.out_dtype, self.H, self.K)
+
+
+class VLayerSet:
+    """L layers of W_UV in one weight format, plus per-M attention outputs x
+    and BF16 results laid out [L, M, H, *]; the V up-projection's LayerSet."""
+
+    def __init__(self, weight_format, n_layers, h=H, m_points=M_POINTS, device="cuda"):
+        import torch
+        from mla_decode_query_gb300 import inputs
+
+        self.weight_format, self.out_dtype, self.L, self.H = weight_format, "bf16", n_layers, h
+        self.m_points = tuple(m_points)
+        ci = V_CONFIG_INDEX[weight_format]
+        m_max = max(32, max(self.m_points))
+        self.host = [inputs.make_v_layer(inputs.layer_seed(ci, l), h, weight_format, m_max=m_max)
+                     for l in range(n_layers)]
+        w = np.stack([d["weight"] for d in self.host])
+        self.weight = torch.from_numpy(w.view(np.int16) if weight_format == "bf16" else w).to(device)
+        self.scale = None
+        if weight_format == "mxfp8":
+            self.scale = torch.from_numpy(np.stack([d["weight_scale"] for d in self.host])).to(device)
+        self.x_host, self.x, self.out = {}, {}, {}
+        for M in self.m_points:
+            self.x_host[M] = torch.from_numpy(np.stack([d["x"][:M] for d in self.host]).view(np.int16)).pin_memory()
+            self.x[M] = self.x_host[M].to(device)
+            self.out[M] = torch.zeros((n_layers, M, h, 128), dtype=torch.int16, device=device)
+
+    def host_inputs(self, M):
+        return [self.x_host[M]]
+
+    def dev_inputs(self, M):
+        return [self.x[M]]
+
+    def kernel_name(self, M):
+        return "mlaqp_v_up_kernel"
+
+    def launch_all(self, M, pdl=True, stream=None):
+        import mla_decode_query_gb300 as mq
+        for l in range(self.L):
+            mq.check(mq.mlaqp_v_up_run(self.x[M][l], self.H * 512, 512, self.weight[l],
+                                       None if self.scale is None else self.scale[l], self.out[M][l],
+                                       128 * self.H, M, self.H, self.weight_format, pdl=pdl, stream=stream))
+
+    def capture(self, M, pdl=True):
+        import torch
+        import mla_decode_query_gb300 as mq
+        mq.check(mq.mlaqp_v_up_prewarm(self.H, max(self.m_points), self.weight_format))
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.launch_all(M, pdl, stream=s)  # untimed eager warm-up
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.launch_all(M, pdl)
+        return g
+
+    def bytes_per_call(self, M):
+        return v_up_algorithmic_bytes(M, self.weight_format, self.H)
 
 
 # --------------------------------------------------------------------------- clocks
@@ -204,10 +285,14 @@ def aggregate_over_ranks(local_ms, local_bytes, world_size, backend_device=None)
 
 # --------------------------------------------------------------------------- CPU oracle timing
 
-def oracle_samples():
+def oracle_samples(op="query"):
     """One layer of each format (layer 0 of its rotated set), host bits."""
     from mla_decode_query_gb300 import inputs
     samples = []
+    if op == "v_up":
+        for fmt, od in V_FORMATS:
+            samples.append((fmt, od, inputs.make_v_layer(inputs.layer_seed(V_CONFIG_INDEX[fmt], 0), H, fmt), None))
+        return samples
     for fmt, od in FORMATS:
         d = inputs.make_layer(inputs.layer_seed(CONFIG_INDEX[fmt], 0), H, fmt)
         qs = inputs.make_q_scale(Q_SCALE_SEED) if od == "e4m3" else None
@@ -215,7 +300,7 @@ def oracle_samples():
     return samples
 
 
-def time_oracle(budget_s, samples, m_points=M_POINTS):
+def time_oracle(budget_s, samples, m_points=M_POINTS, op="query"):
     """Time the oracle, as it stands, on a bounded sample: one layer call per
     (format, M) point, repeated until `budget_s` is spent (at least once).
     Returns (GB/s, calls, seconds)."""
@@ -224,9 +309,13 @@ def time_oracle(budget_s, samples, m_points=M_POINTS):
     while True:
         for fmt, od, d, qs in samples:
             for M in m_points:
-                oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs)
+                if op == "v_up":
+                    oracle.mla_v_up(d["x"][:M], d["weight"], d["weight_scale"], fmt)
+                    nbytes += v_up_algorithmic_bytes(M, fmt)
+                else:
+                    oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs)
+                    nbytes += algorithmic_bytes(M, fmt, od)
                 calls += 1
-                nbytes += algorithmic_bytes(M, fmt, od)
         el = time.perf_counter() - t0
         if el >= budget_s:
             return nbytes / el / 1e9, calls, el
@@ -264,6 +353,10 @@ def run_reference(args):
     return 0
 
 
+METRIC_V = ("achieved HBM GB/s of the MLA V up-projection (W_UV+scales+x+out bytes per layer call / time), "
+            "H=16, M in 1..32, BF16 and MXFP8 W_UV")
+WORKLOAD_V = ("MLA V up-projection, H=16, latent 512 -> v 128; BF16 and MXFP8 W_UV, BF16 out; "
+              "M in {1,2,4,8,16,32}; 128 (BF16) / 256 (MXFP8) rotated layers per CUDA-graph replay")
 METRIC = ("achieved HBM GB/s of the fused MLA decode query projection (weights+scales+q_nope+q_pe+out "
           "bytes per layer call / time), H=16, M in 1..32, BF16 and MXFP8 weights")
 WORKLOAD = ("fused MLA query projection, H=16, K=128, N=512, rope=64; BF16->BF16 and MXFP8->E4M3; "
@@ -287,13 +380,15 @@ def run_gpu(args):
     mq.load_library()
 
     m_points = tuple(int(x) for x in args.m.split(",")) if args.m else M_POINTS
-    formats = [f for f in FORMATS if not args.formats or f[0] in args.formats.split(",")]
+    v_up = args.op == "v_up"
+    formats = [f for f in (V_FORMATS if v_up else FORMATS) if not args.formats or f[0] in args.formats.split(",")]
     if args.pairs:  # explicit weight:output pairs, e.g. bf16:e4m3
         formats = [tuple(x.split(":")) for x in args.pairs.split(",")]
     sets = []
     for fmt, od in formats:
         L = args.layers or DEFAULT_LAYERS[fmt]
-        sets.append(LayerSet(fmt, od, L, m_points=m_points, nope=args.nope))
+        sets.append(VLayerSet(fmt, L, m_points=m_points) if v_up else
+                    LayerSet(fmt, od, L, m_points=m_points, nope=args.nope))
     points = [(s, M) for s in sets for M in m_points]
     graphs = [s.capture(M, pdl=not args.no_pdl) for s, M in points]
     alt = None
@@ -367,14 +462,13 @@ def run_gpu(args):
     launches = args.steps * sum(s.L for s, _ in points)
     dominant = max(kern_ms, key=kern_ms.get)
     ach = kern_bytes[dominant] / (kern_ms[dominant] * 1e-3) / 1e9
-    traffic_table = measured_traffic()
+    traffic_table = None if v_up else measured_traffic()
     traffic = None
     dom_points = [(s, M) for s, M in points if f"{s.weight_format}->{s.out_dtype}" == dominant]
     if traffic_table and all((dominant, M) in traffic_table for _, M in dom_points):
         traffic = round(sum(traffic_table[(dominant, M)] * s.L for s, M in dom_points) /
                         sum(s.L for s, _ in dom_points))
-    kernel_names = sorted({"mlaqp_fused_query_large_kernel" if M > 32 else "mlaqp_fused_query_kernel"
-                           for _, M in dom_points})
+    kernel_names = sorted({s.kernel_name(M) for s, M in dom_points})
     roof = {"bound": "hbm", "kernel": f"{' + '.join(kernel_names)} ({dominant})",
             "achieved": round(ach, 1), "peak": peaks[0], "unit": "GB/s",
             "frac": round(ach / peaks[0], 4), "peak_source": peaks[1], "traffic": traffic,
@@ -384,10 +478,11 @@ def run_gpu(args):
     floor = launch_floor(args.steps, args.warmup)
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "metric": METRIC_V if v_up else METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_name(args.nope, m_points),
+            "config": {"workload": WORKLOAD_V.replace("M in {1,2,4,8,16,32}", "M in {" + ",".join(map(str, m_points)) + "}")
+                       if v_up else workload_name(args.nope, m_points),
                        "heads": H, "nope_dim": args.nope, "m_points": list(m_points),
                        "layers": {s.weight_format: s.L for s in sets}, "pdl": not args.no_pdl,
                        "l2": f"rotated weights per replay {[s.L * s.bytes_per_call(1) >> 20 for s in sets]} MiB "
@@ -402,7 +497,7 @@ def run_gpu(args):
             "e2e": e2e,
         }
         if not args.no_cpu_baseline:
-            gbs, calls, el = time_oracle(args.cpu_budget, oracle_samples())
+            gbs, calls, el = time_oracle(args.cpu_budget, oracle_samples(args.op), op=args.op)
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle_threads(),
                                     "kind": "oracle",
                                     "sample": f"{calls} oracle layer calls over the 12 (format, M) points, "
@@ -420,13 +515,13 @@ def run_e2e(sets, graphs, points, args):
     import torch
     stream = torch.cuda.current_stream()
     host_out = {(id(s), M): torch.empty(s.out[M].shape, dtype=s.out[M].dtype, pin_memory=True) for s, M in points}
-    h2d = sum(s.q_nope_host[M].numel() * 2 + s.q_pe_host[M].numel() * 2 for s, M in points)
+    h2d = sum(t.numel() * t.element_size() for s, M in points for t in s.host_inputs(M))
     d2h = sum(s.out[M].numel() * s.out[M].element_size() for s, M in points)
 
     def step():
         for (s, M), g in zip(points, graphs):
-            s.q_nope[M].copy_(s.q_nope_host[M], non_blocking=True)
-            s.q_pe[M].copy_(s.q_pe_host[M], non_blocking=True)
+            for dst, src in zip(s.dev_inputs(M), s.host_inputs(M)):
+                dst.copy_(src, non_blocking=True)
             g.replay()
             host_out[(id(s), M)].copy_(s.out[M], non_blocking=True)
 
@@ -528,6 +623,8 @@ def main(argv=None):
     ap.add_argument("--formats", type=str, default="", help="comma-separated subset of bf16,mxfp8")
     ap.add_argument("--pairs", type=str, default="", help="comma-separated weight:output pairs, e.g. bf16:e4m3")
     ap.add_argument("--nope", type=int, default=128, choices=(128, 192), help="nope dim (192: GLM shape)")
+    ap.add_argument("--op", choices=["query", "v_up"], default="query",
+                    help="query: the fused query projection (default); v_up: the V up-projection")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--compare-no-pdl", action="store_true", help="also time the graphs without PDL")
     ap.add_argument("--no-e2e", action="store_true")

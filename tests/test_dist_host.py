@@ -65,3 +65,5 @@ def test_bench_bytes_match_oracle_count(M):
     import oracle
     for fmt, od in bench.FORMATS:
         assert bench.algorithmic_bytes(M, fmt, od) == oracle.algorithmic_bytes(M, 16, fmt, od)
+    for fmt, _ in bench.V_FORMATS:
+        assert bench.v_up_algorithmic_bytes(M, fmt) == oracle.v_up_algorithmic_bytes(M, 16, fmt)
