@@ -212,19 +212,28 @@ const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int 
   return &table[nope_idx][out_dtype][mt - 1][trig];
 }
 
-const KernelInfo* lookup_large(int weight_format, int out_dtype, int nope_idx) {
-  return &mlaqp::kernels_large_m()[nope_idx][weight_format][out_dtype];
+// Token tile (tokens per CTA) of a large-M call, as an index into
+// kLargeTokTiles: 32 up to M = 64 (twice the CTAs of a 64-token tile), 64
+// above.
+int large_tile_index(int M) { return M <= 64 ? 0 : 1; }
+
+const KernelInfo* lookup_large(int weight_format, int out_dtype, int nope_idx, int tile_idx) {
+  return &mlaqp::kernels_large_m()[nope_idx][tile_idx][weight_format][out_dtype];
 }
 
-// Chunks of kLargeTokTile tokens of a large-M call (grid.z).
-int large_chunks(int M) { return (M + mlaqp::kLargeTokTile - 1) / mlaqp::kLargeTokTile; }
+// Chunks of one token tile in a large-M call (grid.z).
+int large_chunks(int M) {
+  const int tt = mlaqp::kLargeTokTiles[large_tile_index(M)];
+  return (M + tt - 1) / tt;
+}
 
 // Dynamic shared memory of a large-M launch: the layout's size, padded when
 // needed so that the CTAs one SM can hold never ask for more than its 512
 // TMEM columns between them (a CTA of the largest chunk needs
 // tmem_cols_for(chunk) columns).
 int large_smem(const DeviceInfo& d, int base, int M) {
-  const int chunk = M < mlaqp::kLargeTokTile ? M : mlaqp::kLargeTokTile;
+  const int tt = mlaqp::kLargeTokTiles[large_tile_index(M)];
+  const int chunk = M < tt ? M : tt;
   const int cols = static_cast<int>(mlaqp::tmem_cols_for((chunk + 15) & ~15));
   const int max_ctas = 512 / cols;
   if (d.smem_per_sm / (base + d.reserved_per_block) <= max_ctas) return base;
@@ -242,12 +251,13 @@ int setup_kernels(const DeviceInfo& d) {
         if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
       }
   for (int ki = 0; ki < 2; ++ki)
-    for (int wf = 0; wf < 2; ++wf)
-      for (int od = 0; od < 2; ++od) {
-        const cudaError_t e = cudaFuncSetAttribute(lookup_large(wf, od, ki)->fn,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
-        if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
-      }
+    for (int ti = 0; ti < 2; ++ti)
+      for (int wf = 0; wf < 2; ++wf)
+        for (int od = 0; od < 2; ++od) {
+          const cudaError_t e = cudaFuncSetAttribute(lookup_large(wf, od, ki, ti)->fn,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
+          if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+        }
   const int smem = policy_max_smem(d);
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
@@ -360,7 +370,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   const KernelInfo* k = nullptr;
   int smem_bytes = 0;
   if (large) {
-    k = lookup_large(a.weight_format, a.out_dtype, ki);
+    k = lookup_large(a.weight_format, a.out_dtype, ki, large_tile_index(M));
     smem_bytes = large_smem(g_dev[device], k->smem_bytes, M);
   } else {
     const LaunchPolicy pol = launch_policy(a.weight_format, M);
@@ -568,11 +578,12 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
   }
   const uint32_t large_bit = 1u << (16 + weight_format * 2 + out_dtype);
   if (status == MLAQP_OK && max_m > MLAQP_MAX_M_DECODE && !(g_prewarmed[dev].load(std::memory_order_acquire) & large_bit)) {
-    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki) {
-      cudaFuncAttributes attr;
-      e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki)->fn);
-      if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
-    }
+    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)
+      for (int ti = 0; ti < 2 && status == MLAQP_OK; ++ti) {
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti)->fn);
+        if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
+      }
     if (status == MLAQP_OK) g_prewarmed[dev].fetch_or(large_bit, std::memory_order_acq_rel);
   }
   if (prev != dev) cudaSetDevice(prev);
@@ -608,7 +619,7 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
   if (M > MLAQP_MAX_M_DECODE) {
-    const KernelInfo* k = lookup_large(weight_format, out_dtype, 0);
+    const KernelInfo* k = lookup_large(weight_format, out_dtype, 0, large_tile_index(M));
     if (grid_ctas) *grid_ctas = k->tiles_per_head * H * large_chunks(M);
     if (threads_per_cta) *threads_per_cta = k->threads;
     return MLAQP_OK;

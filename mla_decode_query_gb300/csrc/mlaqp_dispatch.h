@@ -24,10 +24,12 @@ using KernelTable = KernelInfo[2][2][4][kTrigVariants];
 const KernelTable& kernels_bf16_weights();
 const KernelTable& kernels_mxfp8_weights();
 
-// tcgen05 kernels for 32 < M <= 256, [nope][weight_format][out_dtype]; the
-// grid is (tiles_per_head, H, ceil(M / tokens per CTA)) and smem_bytes the
-// unpadded layout size.
-using LargeKernelTable = KernelInfo[2][2][2];
+// tcgen05 kernels for 32 < M <= 256, [nope][token tile][weight_format][out_dtype]
+// with token tiles kLargeTokTiles (tokens per CTA); the grid is
+// (tiles_per_head, H, ceil(M / token tile)) and smem_bytes the unpadded
+// layout size.
+constexpr int kLargeTokTiles[2] = {32, 64};
+using LargeKernelTable = KernelInfo[2][2][2][2];
 const LargeKernelTable& kernels_large_m();
 
 // V up-projection kernels, [weight_format][mt-1][trig] (trig 0: at entry,

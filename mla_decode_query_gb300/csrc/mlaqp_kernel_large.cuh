@@ -36,8 +36,7 @@ namespace mlaqp {
 constexpr int kLargeMaxM = 256;
 constexpr int kLargeNTile = 128;                           // latent columns per CTA (UMMA M)
 constexpr int kLargeTilesPerHead = kLatent / kLargeNTile;  // 4
-constexpr int kLargeThreads = 128;                         // 4 warps = the 128 TMEM lanes
-constexpr int kLargeTokTile = 64;                          // tokens per CTA (grid.z chunks)
+constexpr int kLargeThreads = 256;                         // 2 groups of 4 warps, each spanning the 128 TMEM lanes
 
 // Shared memory layout of the large kernel for nope dim K and TT tokens per
 // CTA (offsets from a 1024-byte aligned base).
@@ -127,23 +126,20 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 32 consecutive FP32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// 16 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  Grid (4, H, ceil(M/TT)); 128 threads.
+// The kernel.  Grid (4, H, ceil(M/TT)); 256 threads.
 // ---------------------------------------------------------------------------
 
 template <int WF, int OD, int K, int TT>
@@ -203,20 +199,20 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
   if (tid < rows) {
 #pragma unroll
     for (int o = 0; o < K; o += 64) prefetch_l2(q_nope + tid * p.q_nope_ts + o);
-  } else if (tid >= 64 && tid - 64 < rows) {
-    prefetch_l2(q_pe + (tid - 64) * p.q_pe_ts);
+  } else if (tid >= 128 && tid - 128 < rows) {
+    prefetch_l2(q_pe + (tid - 128) * p.q_pe_ts);
   }
   uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L.div);
   bool table_ok = false;
   if constexpr (OD == kOutE4M3) {
     table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
-    if (table_ok) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+    if (table_ok && tid < 128) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
   }
   __syncthreads();  // barriers initialised, table visible
 
   // 3. MXFP8: dequantise both 64-column halves into the swizzled BF16 tile
   //    (value = code * 2^(x-127) as two exact power-of-two factors).  Job
-  //    (half, row k, chunk c of 8 columns): 16K jobs, K/8 per thread.
+  //    (half, row k, chunk c of 8 columns): 16K jobs, K/16 per thread.
   if constexpr (WF == kWeightMXFP8) {
     const bool ok = mbar_wait_bounded(bar_w, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
@@ -250,29 +246,37 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
   // 4. Wait for the producer of q_nope / q_pe (no-op without PDL).
   pdl_wait();
 
-  // 5. Accumulator columns in TMEM (warp 0); then the next kernel may launch.
+  // 5. Every input load of the CTA in flight at once: the chunk's q_nope
+  //    rows (rows >= `rows` zero) and its share of the q_pe pairs (the
+  //    chunk's rows*32 pairs dealt over the head's 4 CTAs).
+  constexpr int kPe = (TT * (kRope / 2) + kLargeTilesPerHead * kLargeThreads - 1) / (kLargeTilesPerHead * kLargeThreads);
+  uint4 qv[QI];
+#pragma unroll
+  for (int i = 0; i < QI; ++i) {
+    const int c = tid + kLargeThreads * i;
+    const int m = c / KC;
+    qv[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (m < rows) qv[i] = ld_u128(q_nope + m * p.q_nope_ts + 8 * (c % KC));
+  }
+  uint32_t pe[kPe];
+#pragma unroll
+  for (int i = 0; i < kPe; ++i) {
+    const int j = tile * kLargeThreads + tid + kLargeTilesPerHead * kLargeThreads * i;
+    pe[i] = 0u;
+    if (j < rows * (kRope / 2)) pe[i] = ld_u32(q_pe + (j >> 5) * p.q_pe_ts + 2 * (j & 31));
+  }
+  // Accumulator columns in TMEM (warp 0) while the loads are in flight;
+  // then the next kernel may launch.
   if (warp == 0) tmem_alloc(smem_u32(smem + L.tmem_slot), ncols);
   pdl_launch_dependents();
 
-  // 6. The chunk's q_nope rows into the B tile (all loads, then all stores);
-  //    k slice a of row m, 16-byte chunk cc at a*TT*128 + m*128 + 16*(cc ^ m%8).
-  //    Rows >= rows are zero.
-  {
-    uint4 qv[QI];
+  // 6. q_nope into the B tile: k slice a of row m, 16-byte chunk cc at
+  //    a*TT*128 + m*128 + 16*(cc ^ m%8).
 #pragma unroll
-    for (int i = 0; i < QI; ++i) {
-      const int c = tid + kLargeThreads * i;
-      const int m = c / KC;
-      qv[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (m < rows) qv[i] = ld_u128(q_nope + m * p.q_nope_ts + 8 * (c % KC));
-    }
-#pragma unroll
-    for (int i = 0; i < QI; ++i) {
-      const int c = tid + kLargeThreads * i;
-      const int m = c / KC;
-      const int kc = c % KC;
-      *reinterpret_cast<uint4*>(smem + L.b + (kc >> 3) * (TT * 128) + sw128(m, kc & 7)) = qv[i];
-    }
+  for (int i = 0; i < QI; ++i) {
+    const int c = tid + kLargeThreads * i;
+    const int kc = c % KC;
+    *reinterpret_cast<uint4*>(smem + L.b + (kc >> 3) * (TT * 128) + sw128(c / KC, kc & 7)) = qv[i];
   }
   fence_proxy_async_smem();
   bool ok = true;
@@ -303,35 +307,26 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
     umma_commit(bar_mma);
   }
 
-  // 8. q_pe append while the MMAs run: the chunk's rows*32 value pairs are
-  //    dealt over the head's 4 CTAs (loads first, then the stores).
-  {
-    constexpr int kPe = TT * (kRope / 2) / (kLargeTilesPerHead * kLargeThreads);
-    uint32_t pe[kPe];
+  // 8. q_pe append while the MMAs run (bit copy or E4M3 cast).
 #pragma unroll
-    for (int i = 0; i < kPe; ++i) {
-      const int j = tile * kLargeThreads + tid + kLargeTilesPerHead * kLargeThreads * i;
-      pe[i] = 0u;
-      if (j < rows * (kRope / 2)) pe[i] = ld_u32(q_pe + (j >> 5) * p.q_pe_ts + 2 * (j & 31));
-    }
-#pragma unroll
-    for (int i = 0; i < kPe; ++i) {
-      const int j = tile * kLargeThreads + tid + kLargeTilesPerHead * kLargeThreads * i;
-      if (j < rows * (kRope / 2)) {
-        const size_t off = static_cast<size_t>(m0 + (j >> 5)) * p.out_row_stride + static_cast<size_t>(h) * kOutDim +
-                           kLatent + 2 * (j & 31);
-        if (OD == kOutBF16 || table_ok) {
-          write_pe_pair<OD, true>(p, off, pe[i], divtab, qs);
-        } else {
-          write_pe_pair<OD, false>(p, off, pe[i], divtab, qs);
-        }
+  for (int i = 0; i < kPe; ++i) {
+    const int j = tile * kLargeThreads + tid + kLargeTilesPerHead * kLargeThreads * i;
+    if (j < rows * (kRope / 2)) {
+      const size_t off = static_cast<size_t>(m0 + (j >> 5)) * p.out_row_stride + static_cast<size_t>(h) * kOutDim +
+                         kLatent + 2 * (j & 31);
+      if (OD == kOutBF16 || table_ok) {
+        write_pe_pair<OD, true>(p, off, pe[i], divtab, qs);
+      } else {
+        write_pe_pair<OD, false>(p, off, pe[i], divtab, qs);
       }
     }
   }
 
-  // 9. Epilogue: wait for the accumulator, read this thread's TMEM lane
-  //    (latent column n_cta + 32w + lane) 32 tokens at a time, stage the
-  //    [ntok][128] output tile in the (now free) B region, store its rows.
+  // 9. Epilogue: wait for the accumulator.  Warp w reads TMEM lanes
+  //    32*(w%4).. (latent column n_cta + 32*(w%4) + lane); the two warp
+  //    groups take alternate 16-token column chunks.  Values are rounded to
+  //    BF16 (optionally E4M3), staged as the [ntok][128] output tile in the
+  //    (now free) B region, then stored row by row.
   const bool done = mbar_wait_bounded(bar_mma, 0, p.wait_limit_ns);
   tc_fence_after();
   if (__syncthreads_or(!done)) {
@@ -342,34 +337,33 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
     return;
   }
   constexpr int kEB = OD == kOutBF16 ? 2 : 1;  // output element bytes
-  const int col = 32 * warp + lane;            // latent column within the CTA tile
+  const int quarter = warp & 3;
+  const int col = 32 * quarter + lane;         // latent column within the CTA tile
   uint8_t* stage = smem + L.b;                 // [ntok][128] output elements
-  for (int j0 = 0; j0 < ntok; j0 += 32) {
-    uint32_t r[32];
-    tmem_ld32(taddr + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(j0), r);
-    uint32_t v[16];
+  for (int c16 = warp >> 2; c16 < ntok / 16; c16 += 2) {
+    uint32_t r[16];
+    tmem_ld16(taddr + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(16 * c16), r);
+    uint32_t v[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = pack_bf16x2(__uint_as_float(r[2 * i + 1]), __uint_as_float(r[2 * i]));
+    for (int i = 0; i < 8; ++i) v[i] = pack_bf16x2(__uint_as_float(r[2 * i + 1]), __uint_as_float(r[2 * i]));
     if constexpr (OD == kOutE4M3) {
       if (table_ok) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = e4m3_pair<true>(v[i], divtab, qs);
+        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<true>(v[i], divtab, qs);
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = e4m3_pair<false>(v[i], divtab, qs);
+        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<false>(v[i], divtab, qs);
       }
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int j = j0 + 2 * i;  // tokens j (low half / byte 0) and j+1
-      if (j < ntok) {
-        if constexpr (OD == kOutBF16) {
-          reinterpret_cast<uint16_t*>(stage)[j * kLargeNTile + col] = static_cast<uint16_t>(v[i]);
-          reinterpret_cast<uint16_t*>(stage)[(j + 1) * kLargeNTile + col] = static_cast<uint16_t>(v[i] >> 16);
-        } else {
-          stage[j * kLargeNTile + col] = static_cast<uint8_t>(v[i]);
-          stage[(j + 1) * kLargeNTile + col] = static_cast<uint8_t>(v[i] >> 8);
-        }
+    for (int i = 0; i < 8; ++i) {
+      const int j = 16 * c16 + 2 * i;  // tokens j (low half / byte 0) and j+1
+      if constexpr (OD == kOutBF16) {
+        reinterpret_cast<uint16_t*>(stage)[j * kLargeNTile + col] = static_cast<uint16_t>(v[i]);
+        reinterpret_cast<uint16_t*>(stage)[(j + 1) * kLargeNTile + col] = static_cast<uint16_t>(v[i] >> 16);
+      } else {
+        stage[j * kLargeNTile + col] = static_cast<uint8_t>(v[i]);
+        stage[(j + 1) * kLargeNTile + col] = static_cast<uint8_t>(v[i] >> 8);
       }
     }
   }

@@ -1,30 +1,33 @@
 // Instantiations of the tcgen05 query kernel for 33 <= M <= 256 (both weight
-// formats, both output dtypes, nope dims 128 and 192).
+// formats, both output dtypes, nope dims 128 and 192, 32- and 64-token CTA tiles).
 #include "mlaqp_dispatch.h"
 #include "mlaqp_kernel_large.cuh"
 
 namespace mlaqp {
 namespace {
 
-template <int K, int WF, int OD>
+template <int K, int TT, int WF, int OD>
 KernelInfo entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, kLargeTokTile>),
-                    kLargeThreads, kLargeTilesPerHead, large_smem_layout(K, kLargeTokTile).bytes};
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, TT>), kLargeThreads,
+                    kLargeTilesPerHead, large_smem_layout(K, TT).bytes};
 }
 
-template <int K>
+template <int K, int TT>
 void fill(KernelInfo (&t)[2][2]) {
-  t[kWeightBF16][kOutBF16] = entry<K, kWeightBF16, kOutBF16>();
-  t[kWeightBF16][kOutE4M3] = entry<K, kWeightBF16, kOutE4M3>();
-  t[kWeightMXFP8][kOutBF16] = entry<K, kWeightMXFP8, kOutBF16>();
-  t[kWeightMXFP8][kOutE4M3] = entry<K, kWeightMXFP8, kOutE4M3>();
+  t[kWeightBF16][kOutBF16] = entry<K, TT, kWeightBF16, kOutBF16>();
+  t[kWeightBF16][kOutE4M3] = entry<K, TT, kWeightBF16, kOutE4M3>();
+  t[kWeightMXFP8][kOutBF16] = entry<K, TT, kWeightMXFP8, kOutBF16>();
+  t[kWeightMXFP8][kOutE4M3] = entry<K, TT, kWeightMXFP8, kOutE4M3>();
 }
 
 struct Table {
   LargeKernelTable t;
   Table() {
-    fill<128>(t[0]);
-    fill<192>(t[1]);
+    static_assert(kLargeTokTiles[0] == 32 && kLargeTokTiles[1] == 64, "token tiles");
+    fill<128, 32>(t[0][0]);
+    fill<128, 64>(t[0][1]);
+    fill<192, 32>(t[1][0]);
+    fill<192, 64>(t[1][1]);
   }
 };
 

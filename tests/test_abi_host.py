@@ -103,11 +103,11 @@ def test_launch_shape(built_library):
             st, grid, threads = mq.mlaqp_launch_shape(m, h, "mxfp8", "e4m3")
             # one 4-warp token group up to M=8, two groups above
             assert st == mq.MLAQP_OK and grid == 8 * h and threads == (128 if m <= 8 else 256)
-    # above M = 32: the tcgen05 kernel, 4 CTAs of 128 threads per head and
-    # 64-token chunk
-    for m, chunks in ((33, 1), (64, 1), (65, 2), (200, 4), (256, 4)):
+    # above M = 32: the tcgen05 kernel, 4 CTAs of 256 threads per head and
+    # token chunk (32 tokens up to M = 64, then 64)
+    for m, chunks in ((33, 2), (64, 2), (65, 2), (200, 4), (256, 4)):
         st, grid, threads = mq.mlaqp_launch_shape(m, 11, "bf16", "bf16")
-        assert st == mq.MLAQP_OK and grid == 4 * 11 * chunks and threads == 128
+        assert st == mq.MLAQP_OK and grid == 4 * 11 * chunks and threads == 256
     assert mq.mlaqp_launch_shape(0, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(257, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(4, 12)[0] == mq.MLAQP_ERR_UNSUPPORTED
