@@ -213,9 +213,9 @@ const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int 
 }
 
 // Token tile (tokens per CTA) of a large-M call, as an index into
-// kLargeTokTiles: 32 up to M = 64 (twice the CTAs of a 64-token tile), 64
-// above.
-int large_tile_index(int M) { return M <= 64 ? 0 : 1; }
+// kLargeTokTiles: 32 up to M = 64 (twice the CTAs of a 64-token tile), 64 up
+// to M = 128, 128 above (at most 2 chunks, so one CTA per SM at H = 16).
+int large_tile_index(int M) { return M <= 64 ? 0 : M <= 128 ? 1 : 2; }
 
 const KernelInfo* lookup_large(int weight_format, int out_dtype, int nope_idx, int tile_idx) {
   return &mlaqp::kernels_large_m()[nope_idx][tile_idx][weight_format][out_dtype];
@@ -251,7 +251,7 @@ int setup_kernels(const DeviceInfo& d) {
         if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
       }
   for (int ki = 0; ki < 2; ++ki)
-    for (int ti = 0; ti < 2; ++ti)
+    for (int ti = 0; ti < 3; ++ti)
       for (int wf = 0; wf < 2; ++wf)
         for (int od = 0; od < 2; ++od) {
           const cudaError_t e = cudaFuncSetAttribute(lookup_large(wf, od, ki, ti)->fn,
@@ -579,7 +579,7 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
   const uint32_t large_bit = 1u << (16 + weight_format * 2 + out_dtype);
   if (status == MLAQP_OK && max_m > MLAQP_MAX_M_DECODE && !(g_prewarmed[dev].load(std::memory_order_acquire) & large_bit)) {
     for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)
-      for (int ti = 0; ti < 2 && status == MLAQP_OK; ++ti) {
+      for (int ti = 0; ti < 3 && status == MLAQP_OK; ++ti) {
         cudaFuncAttributes attr;
         e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti)->fn);
         if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);

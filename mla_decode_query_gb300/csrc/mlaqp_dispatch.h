@@ -28,8 +28,8 @@ const KernelTable& kernels_mxfp8_weights();
 // with token tiles kLargeTokTiles (tokens per CTA); the grid is
 // (tiles_per_head, H, ceil(M / token tile)) and smem_bytes the unpadded
 // layout size.
-constexpr int kLargeTokTiles[2] = {32, 64};
-using LargeKernelTable = KernelInfo[2][2][2][2];
+constexpr int kLargeTokTiles[3] = {32, 64, 128};
+using LargeKernelTable = KernelInfo[2][3][2][2];
 const LargeKernelTable& kernels_large_m();
 
 // V up-projection kernels, [weight_format][mt-1][trig] (trig 0: at entry,

@@ -38,27 +38,32 @@ constexpr int kLargeNTile = 128;                           // latent columns per
 constexpr int kLargeTilesPerHead = kLatent / kLargeNTile;  // 4
 constexpr int kLargeThreads = 256;                         // 2 groups of 4 warps, each spanning the 128 TMEM lanes
 
-// Shared memory layout of the large kernel for nope dim K and TT tokens per
-// CTA (offsets from a 1024-byte aligned base).
+// Shared memory layout of the large kernel for nope dim K, TT tokens per CTA
+// and MXFP8 (mx) or BF16 weights (offsets from a 1024-byte aligned base).
+// The E4M3 bytes of an MXFP8 tile share the q_nope region: they are consumed
+// (dequantised into `a`) before the dependency wait, the q_nope rows written
+// after it, with a CTA barrier in between.
 struct LargeSmem {
   int a;          // BF16 weight tile: two [K][64] halves, 128B swizzle
-  int raw;        // MXFP8 only: E4M3 [2][K][64] as copied
-  int scale;      // MXFP8 only: E8M0 [K][16] of the head
   int b;          // q_nope tile: K/64 slices of [TT][64] BF16, 128B swizzle;
                   // after the MMAs, the [ntok][128] output stage
+  int raw;        // MXFP8 only: E4M3 [2][K][64] as copied (= b)
+  int scale;      // MXFP8 only: E8M0 [K][16] of the head
   int div;        // FP32 [128]: RN((128+f)/q_scale)
   int bar;        // two mbarriers: weights, MMA completion
   int tmem_slot;  // TMEM base address written by tcgen05.alloc
   int bytes;      // total, with slack for the 1024-byte alignment
 };
 
-__host__ __device__ constexpr LargeSmem large_smem_layout(int K, int TT) {
+__host__ __device__ constexpr LargeSmem large_smem_layout(int K, int TT, bool mx) {
   LargeSmem s{};
   s.a = 0;
-  s.raw = s.a + 2 * K * 128;
-  s.scale = s.raw + 2 * K * 64;
-  s.b = (s.scale + K * (kLatent / kMxBlock) + 1023) & ~1023;
-  s.div = s.b + TT * K * 2;
+  s.b = s.a + 2 * K * 128;
+  s.raw = s.b;
+  const int bq = TT * K * 2;
+  const int braw = mx ? 2 * K * 64 : 0;
+  s.scale = s.b + (bq > braw ? bq : braw);
+  s.div = s.scale + (mx ? K * (kLatent / kMxBlock) : 0);
   s.bar = s.div + 128 * 4;
   s.tmem_slot = s.bar + 16;
   s.bytes = s.tmem_slot + 16 + 1024;
@@ -146,7 +151,7 @@ template <int WF, int OD, int K, int TT>
 __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(const __grid_constant__ RunParams p) {
   static_assert(K % 64 == 0 && K <= 256, "nope dim: multiple of 64, at most one TMA box (256 rows)");
   static_assert(TT % 16 == 0 && TT <= 256 && (TT * K / 8) % kLargeThreads == 0, "token tile");
-  constexpr LargeSmem L = large_smem_layout(K, TT);
+  constexpr LargeSmem L = large_smem_layout(K, TT, WF == kWeightMXFP8);
   constexpr int KS = K / 16;                          // UMMA k-steps
   constexpr int KC = K / 8;                           // 16-byte chunks per q_nope row
   constexpr int QI = TT * KC / kLargeThreads;         // q_nope chunks per thread
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
       *reinterpret_cast<uint4*>(smem + L.a + half * K * 128 + sw128(k, c)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     fence_proxy_async_smem();
+    __syncthreads();  // every E4M3 byte read before the q_nope rows overwrite them
   }
 
   // 4. Wait for the producer of q_nope / q_pe (no-op without PDL).

@@ -1,5 +1,5 @@
 // Instantiations of the tcgen05 query kernel for 33 <= M <= 256 (both weight
-// formats, both output dtypes, nope dims 128 and 192, 32- and 64-token CTA tiles).
+// formats, both output dtypes, nope dims 128 and 192, 32-, 64- and 128-token CTA tiles).
 #include "mlaqp_dispatch.h"
 #include "mlaqp_kernel_large.cuh"
 
@@ -9,7 +9,7 @@ namespace {
 template <int K, int TT, int WF, int OD>
 KernelInfo entry() {
   return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, TT>), kLargeThreads,
-                    kLargeTilesPerHead, large_smem_layout(K, TT).bytes};
+                    kLargeTilesPerHead, large_smem_layout(K, TT, WF == kWeightMXFP8).bytes};
 }
 
 template <int K, int TT>
@@ -23,11 +23,13 @@ void fill(KernelInfo (&t)[2][2]) {
 struct Table {
   LargeKernelTable t;
   Table() {
-    static_assert(kLargeTokTiles[0] == 32 && kLargeTokTiles[1] == 64, "token tiles");
+    static_assert(kLargeTokTiles[0] == 32 && kLargeTokTiles[1] == 64 && kLargeTokTiles[2] == 128, "token tiles");
     fill<128, 32>(t[0][0]);
     fill<128, 64>(t[0][1]);
+    fill<128, 128>(t[0][2]);
     fill<192, 32>(t[1][0]);
     fill<192, 64>(t[1][1]);
+    fill<192, 128>(t[1][2]);
   }
 };
 

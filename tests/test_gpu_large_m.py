@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 D = 576
 M_MAX = 256
-# chunk edges of the 32- and 64-token CTA tiles, ragged tails, 16-token MMA edges
+# chunk edges of the 32-, 64- and 128-token CTA tiles, ragged tails, 16-token MMA edges
 M_POINTS = (33, 40, 47, 48, 63, 64, 65, 80, 100, 127, 128, 129, 191, 200, 255, 256)
 PAIRS = [("bf16", "bf16"), ("bf16", "e4m3"), ("mxfp8", "bf16"), ("mxfp8", "e4m3")]
 
@@ -58,7 +58,7 @@ def test_domain_and_launch_shape(cuda_device):
             assert mq.mlaqp_prewarm(h, M_MAX, fmt, od) == mq.MLAQP_OK, mq.mlaqp_last_error()
     assert mq.mlaqp_can_implement(16, M_MAX + 1) == 0
     st, grid, threads = mq.mlaqp_launch_shape(200, 16, "bf16", "bf16")
-    assert st == mq.MLAQP_OK and grid == 4 * 16 * 4 and threads == 256
+    assert st == mq.MLAQP_OK and grid == 4 * 16 * 2 and threads == 256
 
 
 @pytest.mark.parametrize("fmt,od", PAIRS)
