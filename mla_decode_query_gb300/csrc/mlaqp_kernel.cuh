@@ -311,13 +311,45 @@ static __device__ __noinline__ uint32_t e4m3_pair_divide(uint32_t two_bf16, floa
   return pack_e4m3x2(__fdiv_rn(bf16_hi(two_bf16), qs), __fdiv_rn(bf16_lo(two_bf16), qs));
 }
 
-// Two BF16 values (packed) -> two E4M3 codes (packed, low value in byte 0)
-// of value / q_scale: IEEE division, then saturating RNE conversion.  The
-// table form has no call and no branch, so the conversions of a thread's
-// values interleave freely; the division form is the out-of-range path.
-template <bool TABLE>
-__device__ __forceinline__ uint32_t e4m3_pair(uint32_t two_bf16, const uint32_t* tab, float qs) {
-  if constexpr (TABLE) {
+// Table form of the exact conversion below (kept out of line: it serves the
+// rare values the multiply cannot decide).
+static __device__ __noinline__ uint32_t e4m3_pair_table(uint32_t two_bf16, const uint32_t* tab) {
+  return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
+}
+
+// True when y = RN(a * RN(1/q_scale)) converts to the same E4M3 code as the
+// IEEE quotient RN(a / q_scale).  With r = RN(1/q_scale) = (1/q_scale)(1+d),
+// |d| <= 2^-24, y = (a/q_scale)(1+d)(1+e), |e| <= 2^-24, so y and RN(a/q_scale)
+// are at most 3 binary32 ulps (of y) apart.  The RNE conversion to E4M3 of a
+// value of magnitude >= 2^-6 (the E4M3 normal range; above 448 both saturate)
+// keeps 3 mantissa bits, so its result changes only across a midpoint, a value
+// whose low 20 mantissa bits are 0x80000.  y qualifies if |y| >= 2^-6 and its
+// low 20 bits are more than 8 from 0x80000; NaN, zero, tiny and near-midpoint
+// values do not, and take the table path.
+__device__ __forceinline__ bool e4m3_mul_decides(float y) {
+  const uint32_t low = __float_as_uint(y) & 0xFFFFFu;
+  return fabsf(y) >= 0x1p-6f && (low - (0x80000u - 8u)) > 16u;
+}
+
+// How a kernel converts value / q_scale to E4M3 (all three give the code of
+// the IEEE binary32 quotient, saturating RNE):
+//   kE4m3Divide: plain IEEE division (q_scale outside [2^-100, 2^100]);
+//   kE4m3Table:  the division table (div_by_table), no branch;
+//   kE4m3Mul:    one multiply by rcp = RN(1/q_scale), exact whenever
+//                e4m3_mul_decides holds, else the table (fewer instructions
+//                per value; the decode kernel keeps the table at M <= 8,
+//                where measurement favours it).
+enum E4m3Mode : int { kE4m3Divide = 0, kE4m3Table = 1, kE4m3Mul = 2 };
+
+// Two BF16 values (packed) -> two E4M3 codes (packed, low value in byte 0).
+template <int MODE>
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t two_bf16, const uint32_t* tab, float qs, float rcp) {
+  if constexpr (MODE == kE4m3Mul) {
+    const float hi = __fmul_rn(bf16_hi(two_bf16), rcp);
+    const float lo = __fmul_rn(bf16_lo(two_bf16), rcp);
+    if (e4m3_mul_decides(hi) && e4m3_mul_decides(lo)) return pack_e4m3x2(hi, lo);
+    return e4m3_pair_table(two_bf16, tab);
+  } else if constexpr (MODE == kE4m3Table) {
     return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
   } else {
     return e4m3_pair_divide(two_bf16, qs);
@@ -344,9 +376,10 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // movmatrix.trans a lane holds token 8jt+g and columns 16w+2t, +1 (first
 // block) and 16w+8+2t, +1 (second block); stores go straight to
 // out[m*row_stride + h*576 + n].
-template <int OD, int MTW, int TS, bool TABLE>
+template <int OD, int MTW, int TS, int MODE>
 __device__ __forceinline__ void write_projection(const RunParams& p, const float (&acc)[MTW][4], int wcol, int wtok,
-                                                 int lane, int h, int n_cta, const uint32_t* divtab, float qs) {
+                                                 int lane, int h, int n_cta, const uint32_t* divtab, float qs,
+                                                 float rcp) {
   constexpr int MT = MTW;  // this warp's token tiles: jt = wtok + TS*i, i < MTW
   const int g = lane >> 2;
   const int t = lane & 3;
@@ -361,8 +394,8 @@ __device__ __forceinline__ void write_projection(const RunParams& p, const float
   if constexpr (OD == kOutE4M3) {
 #pragma unroll
     for (int jt = 0; jt < MT; ++jt) {
-      r[jt][0] = e4m3_pair<TABLE>(r[jt][0], divtab, qs);
-      r[jt][1] = e4m3_pair<TABLE>(r[jt][1], divtab, qs);
+      r[jt][0] = e4m3_pair<MODE>(r[jt][0], divtab, qs, rcp);
+      r[jt][1] = e4m3_pair<MODE>(r[jt][1], divtab, qs, rcp);
     }
   }
 #pragma unroll
@@ -386,13 +419,13 @@ __device__ __forceinline__ void write_projection(const RunParams& p, const float
 
 // Step 8: the q_pe append for one pair of values (2 BF16 in, 2 BF16 or
 // 2 E4M3 out) at element offset `off` of the output.
-template <int OD, bool TABLE>
+template <int OD, int MODE>
 __device__ __forceinline__ void write_pe_pair(const RunParams& p, size_t off, uint32_t pe2, const uint32_t* divtab,
-                                              float qs) {
+                                              float qs, float rcp) {
   if constexpr (OD == kOutBF16) {
     *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + off) = pe2;
   } else {
-    *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<TABLE>(pe2, divtab, qs));
+    *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<MODE>(pe2, divtab, qs, rcp));
   }
 }
 
@@ -412,6 +445,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   constexpr int MTW = (MT + TS - 1) / TS;   // token tiles per warp
   constexpr int KS = K / 16;                // MMA k-steps
   constexpr int KC = K / 8;                 // 16-byte chunks per q_nope row
+  constexpr int kTableMode = MT >= 2 ? kE4m3Mul : kE4m3Table;  // E4M3 conversion with the table available
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_a = smem_u32(smem + L::A);
@@ -522,9 +556,11 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   // visible by the barrier after the q_nope tile is stored.
   uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L::Div);
   bool table_ok = false;
+  float rcp = 1.f;
   if constexpr (OD == kOutE4M3) {
     table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
     if (table_ok && tid < 128) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+    rcp = __frcp_rn(qs);
   }
 
   // 4. Wait for the producer of q_nope / q_pe (no-op without PDL).
@@ -579,9 +615,9 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     const size_t off = static_cast<size_t>(m_pe) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + kLatent +
                        2 * (j_pe & 31);
     if (OD == kOutBF16 || table_ok) {
-      write_pe_pair<OD, true>(p, off, pe, divtab, qs);
+      write_pe_pair<OD, kTableMode>(p, off, pe, divtab, qs, rcp);
     } else {
-      write_pe_pair<OD, false>(p, off, pe, divtab, qs);
+      write_pe_pair<OD, kE4m3Divide>(p, off, pe, divtab, qs, rcp);
     }
   }
 
@@ -617,11 +653,11 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   // 7. Epilogue; the E4M3 division form is chosen once per CTA so that the
   //    common path holds no call and no branch.
   if constexpr (OD == kOutBF16) {
-    write_projection<OD, MTW, TS, true>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs);
+    write_projection<OD, MTW, TS, kTableMode>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
   } else if (table_ok) {
-    write_projection<OD, MTW, TS, true>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs);
+    write_projection<OD, MTW, TS, kTableMode>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
   } else {
-    write_projection<OD, MTW, TS, false>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs);
+    write_projection<OD, MTW, TS, kE4m3Divide>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
   }
 }
 

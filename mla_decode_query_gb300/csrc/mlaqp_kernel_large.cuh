@@ -209,9 +209,11 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
   }
   uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L.div);
   bool table_ok = false;
+  float rcp = 1.f;
   if constexpr (OD == kOutE4M3) {
     table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
     if (table_ok && tid < 128) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+    rcp = __frcp_rn(qs);
   }
   __syncthreads();  // barriers initialised, table visible
 
@@ -321,9 +323,9 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
       const size_t off = static_cast<size_t>(m0 + (j >> 5)) * p.out_row_stride + static_cast<size_t>(h) * kOutDim +
                          kLatent + 2 * (j & 31);
       if (OD == kOutBF16 || table_ok) {
-        write_pe_pair<OD, true>(p, off, pe[i], divtab, qs);
+        write_pe_pair<OD, kE4m3Mul>(p, off, pe[i], divtab, qs, rcp);
       } else {
-        write_pe_pair<OD, false>(p, off, pe[i], divtab, qs);
+        write_pe_pair<OD, kE4m3Divide>(p, off, pe[i], divtab, qs, rcp);
       }
     }
   }
@@ -355,10 +357,10 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
     if constexpr (OD == kOutE4M3) {
       if (table_ok) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<true>(v[i], divtab, qs);
+        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<kE4m3Mul>(v[i], divtab, qs, rcp);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<false>(v[i], divtab, qs);
+        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<kE4m3Divide>(v[i], divtab, qs, rcp);
       }
     }
 #pragma unroll

@@ -184,14 +184,16 @@ def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device):
         assert word == 0
 
 
+@pytest.mark.parametrize("M", [8, 32, 64])
 @pytest.mark.parametrize("qs", [0.01, 0.0371, 0.1, 3.0, 1e-20, 1e20, 2.0 ** -110, 2.0 ** 110])
-def test_e4m3_division_every_bf16_value(cuda_device, qs):
+def test_e4m3_division_every_bf16_value(cuda_device, qs, M):
     # The q_pe columns of an E4M3 output are e4m3_satfinite(q_pe / q_scale):
     # feed every non-NaN BF16 bit pattern through them and require the codes
-    # bit for bit.  The scales cover the kernel's exact table path, results
-    # that overflow or underflow binary32, and q_scale outside 2^-100..2^100
-    # (plain division).
-    H, M = 16, 32
+    # bit for bit.  The scales cover the kernels' exact table and multiply
+    # paths (M = 8: decode kernel, table; M = 32: decode kernel, multiply;
+    # M = 64: tcgen05 kernel, multiply), results that overflow or underflow
+    # binary32, and q_scale outside 2^-100..2^100 (plain division).
+    H = 16
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # drop inf / NaN patterns
     per_call = M * H * 64
