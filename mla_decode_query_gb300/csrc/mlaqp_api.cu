@@ -163,25 +163,32 @@ int encode_weight_map(CUtensorMap* map, const void* weight, int H, int K, bool m
 // Launch policy of one call: where a PDL-launched CTA lets the next kernel
 // start (see the kernel) and an optional cap on resident CTAs per SM,
 // imposed by padding the dynamic shared memory.  Chosen from per-layer times
-// of 128-layer CUDA-graph chains on GB300:
-//   * BF16 weights, M <= 8: trigger at entry, at most 3 CTAs per SM -- the
-//     weight stream overlaps the previous layers while early-launched
-//     kernels cannot crowd many of their CTAs onto a few SMs;
-//   * BF16 weights, M > 8: trigger after the dependency wait (two kernels in
-//     flight, one CTA per SM), since the heavier epilogue suffers most when
-//     CTAs share an SM;
-//   * MXFP8 weights need their copy and dequantisation ahead of the wait:
-//     entry trigger, uncapped for M <= 4 and capped at 3 CTAs per SM up to
-//     M = 16; after the wait for M > 16.
+// of 128-layer CUDA-graph chains on GB300 (H = 16): the query kernel
+// triggers at entry with at most 2 CTAs per SM at every M.  One layer then
+// runs ahead with its weight copy (and MXFP8 dequantisation) overlapped,
+// while no SM holds more than one early-launched CTA next to the running
+// one.  Against the earlier mix (cap 3 up to M = 8, MXFP8 uncapped up to
+// M = 4, trigger after the wait above M = 16), MXFP8->E4M3 went from
+// 1.62 / 1.82 / 2.84 us to 1.38 / 1.52 / 2.54 us at M = 1 / 8 / 32.  The V
+// up-projection uses the same policy except BF16 above M = 16, which
+// triggers after the wait (2.37 against 2.94 us at M = 32).
 struct LaunchPolicy {
   int trig;     // 0 entry, 1 after the wait, 2 weights ready
   int cta_cap;  // 0: none, else resident CTAs per SM
 };
 
+// Smallest CTA cap any policy uses (the largest padded shared memory).
+constexpr int kMinCtaCap = 2;
+
 LaunchPolicy launch_policy(int weight_format, int M) {
-  if (weight_format == MLAQP_WEIGHT_BF16) return M <= 8 ? LaunchPolicy{0, 3} : LaunchPolicy{1, 0};
-  if (M <= 4) return LaunchPolicy{0, 0};
-  return M <= 16 ? LaunchPolicy{0, 3} : LaunchPolicy{1, 0};
+  (void)weight_format;
+  (void)M;
+  return LaunchPolicy{0, 2};
+}
+
+LaunchPolicy v_up_launch_policy(int weight_format, int M) {
+  if (weight_format == MLAQP_WEIGHT_BF16 && M > 16) return LaunchPolicy{1, 0};
+  return LaunchPolicy{0, 2};
 }
 
 // Dynamic shared memory that realises `cap` CTAs per SM for a kernel that
@@ -194,7 +201,7 @@ int smem_for_cap(const DeviceInfo& d, int base, int cap) {
 
 int policy_max_smem(const DeviceInfo& d) {
   const int base = mlaqp::Smem<128>::Bytes > mlaqp::Smem<192>::Bytes ? mlaqp::Smem<128>::Bytes : mlaqp::Smem<192>::Bytes;
-  return smem_for_cap(d, base, 3);
+  return smem_for_cap(d, base, kMinCtaCap);
 }
 
 // Index of a supported nope dim in the kernel tables, or -1.
@@ -247,7 +254,7 @@ int setup_kernels(const DeviceInfo& d) {
       for (int trig = 0; trig < 2; ++trig) {
         const KernelInfo& k = mlaqp::kernels_v_up()[wf][mt][trig];
         const cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   smem_for_cap(d, k.smem_bytes, 3));
+                                                   smem_for_cap(d, k.smem_bytes, kMinCtaCap));
         if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
       }
   for (int ki = 0; ki < 2; ++ki)
@@ -488,9 +495,7 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long l
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  // Same trigger / CTA-cap policy as the query kernel (same CTA count per
-  // head, similar per-CTA weight tile).
-  const LaunchPolicy pol = launch_policy(a.weight_format, M);
+  const LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
   const KernelInfo* k = lookup_v_up(a.weight_format, M, pol.trig == 0 ? 0 : 1);
   const int smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   mlaqp::VUpParams params;
