@@ -169,9 +169,11 @@ int encode_weight_map(CUtensorMap* map, const void* weight, int H, int K, bool m
 // while no SM holds more than one early-launched CTA next to the running
 // one.  Against the earlier mix (cap 3 up to M = 8, MXFP8 uncapped up to
 // M = 4, trigger after the wait above M = 16), MXFP8->E4M3 went from
-// 1.62 / 1.82 / 2.84 us to 1.38 / 1.52 / 2.54 us at M = 1 / 8 / 32.  The V
-// up-projection uses the same policy except BF16 above M = 16, which
-// triggers after the wait (2.37 against 2.94 us at M = 32).
+// 1.62 / 1.82 / 2.84 us to 1.38 / 1.52 / 2.54 us at M = 1 / 8 / 32.  The
+// exception is BF16 weights with E4M3 output above M = 16, which trigger
+// after the wait (2.16 against 2.61 us at M = 32); the V up-projection
+// likewise triggers after the wait for BF16 weights above M = 16 (2.37
+// against 2.94 us at M = 32).
 struct LaunchPolicy {
   int trig;     // 0 entry, 1 after the wait, 2 weights ready
   int cta_cap;  // 0: none, else resident CTAs per SM
@@ -180,9 +182,8 @@ struct LaunchPolicy {
 // Smallest CTA cap any policy uses (the largest padded shared memory).
 constexpr int kMinCtaCap = 2;
 
-LaunchPolicy launch_policy(int weight_format, int M) {
-  (void)weight_format;
-  (void)M;
+LaunchPolicy launch_policy(int weight_format, int out_dtype, int M) {
+  if (weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3 && M > 16) return LaunchPolicy{1, 0};
   return LaunchPolicy{0, 2};
 }
 
@@ -380,7 +381,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
     k = lookup_large(a.weight_format, a.out_dtype, ki, large_tile_index(M));
     smem_bytes = large_smem(g_dev[device], k->smem_bytes, M);
   } else {
-    const LaunchPolicy pol = launch_policy(a.weight_format, M);
+    const LaunchPolicy pol = launch_policy(a.weight_format, a.out_dtype, M);
     k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki);
     smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   }
@@ -629,7 +630,7 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
     if (threads_per_cta) *threads_per_cta = k->threads;
     return MLAQP_OK;
   }
-  const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, M).trig, 0);
+  const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0);
   if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
   if (threads_per_cta) *threads_per_cta = k->threads;
   return MLAQP_OK;
