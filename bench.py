@@ -462,7 +462,7 @@ def run_gpu(args):
     launches = args.steps * sum(s.L for s, _ in points)
     dominant = max(kern_ms, key=kern_ms.get)
     ach = kern_bytes[dominant] / (kern_ms[dominant] * 1e-3) / 1e9
-    traffic_table = None if v_up else measured_traffic()
+    traffic_table = None if (v_up or args.nope != 128) else measured_traffic()  # the table covers K = 128
     traffic = None
     dom_points = [(s, M) for s, M in points if f"{s.weight_format}->{s.out_dtype}" == dominant]
     if traffic_table and all((dominant, M) in traffic_table for _, M in dom_points):
