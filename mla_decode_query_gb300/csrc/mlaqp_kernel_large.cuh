@@ -36,7 +36,8 @@ namespace mlaqp {
 constexpr int kLargeMaxM = 256;
 constexpr int kLargeNTile = 128;                           // latent columns per CTA (UMMA M)
 constexpr int kLargeTilesPerHead = kLatent / kLargeNTile;  // 4
-constexpr int kLargeThreads = 256;                         // 2 groups of 4 warps, each spanning the 128 TMEM lanes
+constexpr int kLargeThreads = 256;                         // groups of 4 warps, each spanning the 128 TMEM lanes
+constexpr int kLargeGroups = kLargeThreads / 128;
 
 // Shared memory layout of the large kernel for nope dim K, TT tokens per CTA
 // and MXFP8 (mx) or BF16 weights (offsets from a 1024-byte aligned base).
@@ -204,8 +205,9 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
   if (tid < rows) {
 #pragma unroll
     for (int o = 0; o < K; o += 64) prefetch_l2(q_nope + tid * p.q_nope_ts + o);
-  } else if (tid >= 128 && tid - 128 < rows) {
-    prefetch_l2(q_pe + (tid - 128) * p.q_pe_ts);
+  }
+  if (tid >= kLargeThreads - 128 && tid - (kLargeThreads - 128) < rows) {
+    prefetch_l2(q_pe + (tid - (kLargeThreads - 128)) * p.q_pe_ts);
   }
   uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L.div);
   bool table_ok = false;
@@ -331,8 +333,8 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
   }
 
   // 9. Epilogue: wait for the accumulator.  Warp w reads TMEM lanes
-  //    32*(w%4).. (latent column n_cta + 32*(w%4) + lane); the two warp
-  //    groups take alternate 16-token column chunks.  Values are rounded to
+  //    32*(w%4).. (latent column n_cta + 32*(w%4) + lane); the warp groups
+  //    take the 16-token column chunks in turn.  Values are rounded to
   //    BF16 (optionally E4M3), staged as the [ntok][128] output tile in the
   //    (now free) B region, then stored row by row.
   const bool done = mbar_wait_bounded(bar_mma, 0, p.wait_limit_ns);
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(kLargeThreads) mlaqp_fused_query_large_kernel(
   const int quarter = warp & 3;
   const int col = 32 * quarter + lane;         // latent column within the CTA tile
   uint8_t* stage = smem + L.b;                 // [ntok][128] output elements
-  for (int c16 = warp >> 2; c16 < ntok / 16; c16 += 2) {
+  for (int c16 = warp >> 2; c16 < ntok / 16; c16 += kLargeGroups) {
     uint32_t r[16];
     tmem_ld16(taddr + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(16 * c16), r);
     uint32_t v[8];

@@ -218,3 +218,33 @@ def test_e4m3_saturation_and_plain_division(cuda_device, qs):
     got = _rows(_run(_dev(d), M, H, "mxfp8", "e4m3", qs), M, H, D * H, "e4m3")
     ref, acc = _oracle(d, "mxfp8", "e4m3", qs)
     check_output(got, ref, acc, "e4m3", f"qs={qs}")
+
+
+@pytest.mark.parametrize("K", [128, 192])
+def test_strided_and_head_major_inputs(cuda_device, K):
+    # The tcgen05 kernel reads q_nope / q_pe through token and head strides:
+    # views into the upstream [M, H, K+64] projection, and a head-major
+    # [H, M, K] q_nope with a head-major [H, M, 64] q_pe.
+    H = 16
+    for fmt, od in (("bf16", "bf16"), ("mxfp8", "e4m3")):
+        d = inputs.make_layer(inputs.layer_seed(38, K), H, fmt, m_max=M_MAX, nope=K)
+        qs = inputs.make_q_scale(38) if od == "e4m3" else None
+        ref, acc = _oracle(d, fmt, od, qs)
+        w = to_device(d["weight"])
+        sc = None if d["weight_scale"] is None else to_device(d["weight_scale"])
+        q_scale = None if qs is None else torch.tensor([qs], dtype=torch.float32, device="cuda")
+        up = np.concatenate([d["q_nope"], d["q_pe"]], axis=-1)  # [M, H, K+64]
+        upd = to_device(up)
+        qn_hm = to_device(np.ascontiguousarray(np.transpose(d["q_nope"], (1, 0, 2))))
+        qp_hm = to_device(np.ascontiguousarray(np.transpose(d["q_pe"], (1, 0, 2))))
+        for M in (33, 100, 256):
+            for name, args in (
+                ("upstream view", (upd, H * (K + 64), K + 64, upd[..., K:], H * (K + 64), K + 64)),
+                ("head-major", (qn_hm, K, M_MAX * K, qp_hm, 64, M_MAX * 64)),
+            ):
+                out = torch.zeros((M * D * H,), dtype=torch.int16 if od == "bf16" else torch.uint8, device="cuda")
+                st = mq.mlaqp_run_strided(args[0], args[1], args[2], args[3], args[4], args[5], w, sc, out, D * H,
+                                          q_scale, M, H, K, fmt, od, pdl=(M == 100))
+                assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
+                torch.cuda.synchronize()
+                check_output(_rows(out, M, H, D * H, od), ref[:M], acc[:M], od, f"K{K} {fmt}->{od} M{M} {name}")
