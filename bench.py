@@ -509,35 +509,66 @@ def run_gpu(args):
 
 
 def run_e2e(sets, graphs, points, args):
-    """Same metric through the public API with host buffers: per step, copy
-    every point's q_nope / q_pe from pinned host memory, replay, copy the
-    outputs back to pinned host memory."""
+    """Same metric through the public API with host buffers.  Every step
+    copies every point's q_nope / q_pe from pinned host memory, replays the
+    point's graph and copies its outputs back to pinned host memory.  The
+    copies run on their own streams, so point i+1's inputs travel while point
+    i computes and point i's outputs travel while point i+1 computes; events
+    keep each buffer's copy-in, use and copy-out in order, across steps too.
+    The timed region runs from before the first copy to after the last
+    copy-out of the last step."""
     import torch
-    stream = torch.cuda.current_stream()
-    host_out = {(id(s), M): torch.empty(s.out[M].shape, dtype=s.out[M].dtype, pin_memory=True) for s, M in points}
+    comp = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    n = len(points)
+    host_out = [torch.empty(s.out[M].shape, dtype=s.out[M].dtype, pin_memory=True) for s, M in points]
     h2d = sum(t.numel() * t.element_size() for s, M in points for t in s.host_inputs(M))
     d2h = sum(s.out[M].numel() * s.out[M].element_size() for s, M in points)
+    in_ready = [torch.cuda.Event() for _ in range(n)]  # point i's inputs are on the device
+    computed = [torch.cuda.Event() for _ in range(n)]  # point i's graph has run (inputs read, outputs written)
+    out_read = [torch.cuda.Event() for _ in range(n)]  # point i's outputs are on the host
+    started = [False]
 
     def step():
-        for (s, M), g in zip(points, graphs):
-            for dst, src in zip(s.dev_inputs(M), s.host_inputs(M)):
-                dst.copy_(src, non_blocking=True)
+        for i, ((s, M), g) in enumerate(zip(points, graphs)):
+            if started[0]:
+                h2d_s.wait_event(computed[i])  # the previous step's replay of i has read its inputs
+            with torch.cuda.stream(h2d_s):
+                for dst, src in zip(s.dev_inputs(M), s.host_inputs(M)):
+                    dst.copy_(src, non_blocking=True)
+            in_ready[i].record(h2d_s)
+            comp.wait_event(in_ready[i])
+            if started[0]:
+                comp.wait_event(out_read[i])  # the previous step's outputs of i have left the device
             g.replay()
-            host_out[(id(s), M)].copy_(s.out[M], non_blocking=True)
+            computed[i].record(comp)
+            d2h_s.wait_event(computed[i])
+            with torch.cuda.stream(d2h_s):
+                host_out[i].copy_(s.out[M], non_blocking=True)
+            out_read[i].record(d2h_s)
+        started[0] = True
 
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(comp)
+    h2d_s.wait_event(a)
+    d2h_s.wait_event(a)
     for _ in range(args.steps):
         step()
-    b.record(stream)
+    comp.wait_stream(h2d_s)
+    comp.wait_stream(d2h_s)
+    b.record(comp)
     torch.cuda.synchronize()
+    for i, (s, M) in enumerate(points):  # the host copies hold the last step's outputs
+        if not torch.equal(host_out[i], s.out[M].cpu()):
+            raise RuntimeError(f"e2e: host copy of point {i} differs from the device output")
     ms = a.elapsed_time(b)
     nbytes = sum(s.bytes_per_call(M) * s.L for s, M in points) * args.steps
     return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms / args.steps, 4)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms / args.steps, 4),
+            "copies": "pinned host <-> device on two copy streams, overlapped with the previous / next point's replay"}
 
 
 KERNEL_SOURCES = ("mla_decode_query_gb300/csrc/mlaqp_kernel.cuh", "mla_decode_query_gb300/csrc/mlaqp_kernels_bf16.cu",
