@@ -24,9 +24,15 @@ same workload on the host cores (the only other code path this file runs).
 
 from __future__ import annotations
 
+import os
+
+# The CPU oracle legs report one core: keep numpy's BLAS single-threaded (set
+# before numpy loads it).
+os.environ["OPENBLAS_NUM_THREADS"] = "1"
+os.environ["MKL_NUM_THREADS"] = "1"
+
 import argparse
 import json
-import os
 import statistics
 import subprocess
 import sys
@@ -39,6 +45,14 @@ H = 16
 M_POINTS = (1, 2, 4, 8, 16, 32)
 FORMATS = (("bf16", "bf16"), ("mxfp8", "e4m3"))
 DEFAULT_LAYERS = {"bf16": 128, "mxfp8": 256}
+
+
+def layers_for(fmt, h, v_up=False):
+    """Rotated layers per graph: the H=16 defaults, raised for fewer heads so
+    that the weights of one replay stay at least twice the L2 size."""
+    per_layer = h * 512 * 128 * (2 if fmt == "bf16" else 1)
+    need = -(-2 * L2_BYTES // per_layer)
+    return max(DEFAULT_LAYERS[fmt], -(-need // 32) * 32)
 CONFIG_INDEX = {"bf16": 1, "mxfp8": 3}  # seed family 1000*i + layer
 V_CONFIG_INDEX = {"bf16": 6, "mxfp8": 7}
 V_FORMATS = (("bf16", "bf16"), ("mxfp8", "bf16"))
@@ -363,8 +377,17 @@ WORKLOAD = ("fused MLA query projection, H=16, K=128, N=512, rope=64; BF16->BF16
             "M in {1,2,4,8,16,32}; 128 (BF16) / 256 (MXFP8) rotated layers per CUDA-graph replay")
 
 
-def workload_name(nope, m_points):
-    w = WORKLOAD.replace("M in {1,2,4,8,16,32}", "M in {" + ",".join(map(str, m_points)) + "}")
+def workload_name(nope, m_points, heads=(16,), formats=FORMATS, v_up=False):
+    """The workload of a run, named by what it is; the default run's name is WORKLOAD."""
+    w = WORKLOAD_V if v_up else WORKLOAD
+    w = w.replace("M in {1,2,4,8,16,32}", "M in {" + ",".join(map(str, m_points)) + "}")
+    if tuple(heads) != (16,):
+        w = w.replace("H=16", "H in {" + ",".join(map(str, heads)) + "}")
+    if not v_up and tuple(formats) != FORMATS:
+        w = w.replace("BF16->BF16 and MXFP8->E4M3",
+                      ", ".join(f"{a.upper()}->{b.upper()}" for a, b in formats))
+    if not v_up and (tuple(heads) != (16,)):
+        w = w.replace("128 (BF16) / 256 (MXFP8) rotated layers", "rotated layers (at least 2x L2 of weights)")
     return w if nope == 128 else w.replace("K=128", f"K={nope}")
 
 
@@ -384,11 +407,17 @@ def run_gpu(args):
     formats = [f for f in (V_FORMATS if v_up else FORMATS) if not args.formats or f[0] in args.formats.split(",")]
     if args.pairs:  # explicit weight:output pairs, e.g. bf16:e4m3
         formats = [tuple(x.split(":")) for x in args.pairs.split(",")]
+    heads = tuple(int(x) for x in args.heads.split(","))
+    multi = len(heads) > 1
     sets = []
-    for fmt, od in formats:
-        L = args.layers or DEFAULT_LAYERS[fmt]
-        sets.append(VLayerSet(fmt, L, m_points=m_points) if v_up else
-                    LayerSet(fmt, od, L, m_points=m_points, nope=args.nope))
+    for h in heads:
+        for fmt, od in formats:
+            L = args.layers or layers_for(fmt, h, v_up)
+            sets.append(VLayerSet(fmt, L, h=h, m_points=m_points) if v_up else
+                        LayerSet(fmt, od, L, h=h, m_points=m_points, nope=args.nope))
+
+    def key(s):
+        return f"{s.weight_format}->{s.out_dtype}" + (f" H{s.H}" if multi else "")
     points = [(s, M) for s in sets for M in m_points]
     graphs = [s.capture(M, pdl=not args.no_pdl) for s, M in points]
     alt = None
@@ -430,18 +459,18 @@ def run_gpu(args):
     value = total_bytes / (total_ms * 1e-3) / 1e9
 
     per_point = []
-    kern_ms = {f"{fmt}->{od}": 0.0 for fmt, od in formats}
-    kern_bytes = {f"{fmt}->{od}": 0 for fmt, od in formats}
+    kern_ms = {key(s): 0.0 for s in sets}
+    kern_bytes = {key(s): 0 for s in sets}
     for i, (s, M) in enumerate(points):
         ms = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
         med = statistics.median(ms)
         us = 1e3 * med / s.L
-        per_point.append({"weights": s.weight_format, "out": s.out_dtype, "M": M, "layers": s.L,
-                          "us_per_layer": round(us, 4),
+        p10, p90 = (1e3 * float(np.percentile(ms, q)) / s.L for q in (10, 90))
+        per_point.append({"weights": s.weight_format, "out": s.out_dtype, "H": s.H, "M": M, "layers": s.L,
+                          "us_per_layer": round(us, 4), "us_p10": round(p10, 4), "us_p90": round(p90, 4),
                           "gbs": round(s.bytes_per_call(M) / (us * 1e-6) / 1e9, 1)})
-        key = f"{s.weight_format}->{s.out_dtype}"
-        kern_ms[key] += sum(ms)
-        kern_bytes[key] += s.bytes_per_call(M) * s.L * args.steps
+        kern_ms[key(s)] += sum(ms)
+        kern_bytes[key(s)] += s.bytes_per_call(M) * s.L * args.steps
 
     if alt is not None:  # context: the same graphs launched without PDL (plain stream order)
         for i, (s, M) in enumerate(points):
@@ -462,9 +491,9 @@ def run_gpu(args):
     launches = args.steps * sum(s.L for s, _ in points)
     dominant = max(kern_ms, key=kern_ms.get)
     ach = kern_bytes[dominant] / (kern_ms[dominant] * 1e-3) / 1e9
-    traffic_table = None if (v_up or args.nope != 128) else measured_traffic()  # the table covers K = 128
+    traffic_table = None if (v_up or args.nope != 128 or heads != (16,)) else measured_traffic()  # K=128, H=16
     traffic = None
-    dom_points = [(s, M) for s, M in points if f"{s.weight_format}->{s.out_dtype}" == dominant]
+    dom_points = [(s, M) for s, M in points if key(s) == dominant]
     if traffic_table and all((dominant, M) in traffic_table for _, M in dom_points):
         traffic = round(sum(traffic_table[(dominant, M)] * s.L for s, M in dom_points) /
                         sum(s.L for s, _ in dom_points))
@@ -481,10 +510,10 @@ def run_gpu(args):
             "metric": METRIC_V if v_up else METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD_V.replace("M in {1,2,4,8,16,32}", "M in {" + ",".join(map(str, m_points)) + "}")
-                       if v_up else workload_name(args.nope, m_points),
-                       "heads": H, "nope_dim": args.nope, "m_points": list(m_points),
-                       "layers": {s.weight_format: s.L for s in sets}, "pdl": not args.no_pdl,
+            "config": {"workload": workload_name(args.nope, m_points, heads, tuple(formats), v_up),
+                       "heads": heads[0] if not multi else list(heads), "nope_dim": args.nope,
+                       "m_points": list(m_points),
+                       "layers": {key(s): s.L for s in sets}, "pdl": not args.no_pdl,
                        "l2": f"rotated weights per replay {[s.L * s.bytes_per_call(1) >> 20 for s in sets]} MiB "
                              f"vs L2 {L2_BYTES >> 20} MiB (inputs larger than L2, no flush)",
                        "parallelism": f"replicas{ws}"},
@@ -654,6 +683,7 @@ def main(argv=None):
     ap.add_argument("--formats", type=str, default="", help="comma-separated subset of bf16,mxfp8")
     ap.add_argument("--pairs", type=str, default="", help="comma-separated weight:output pairs, e.g. bf16:e4m3")
     ap.add_argument("--nope", type=int, default=128, choices=(128, 192), help="nope dim (192: GLM shape)")
+    ap.add_argument("--heads", type=str, default="16", help="comma-separated head counts (8, 11, 16)")
     ap.add_argument("--op", choices=["query", "v_up"], default="query",
                     help="query: the fused query projection (default); v_up: the V up-projection")
     ap.add_argument("--no-pdl", action="store_true")
