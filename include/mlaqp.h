@@ -132,14 +132,17 @@ int mlaqp_run(const void* q_nope, const void* q_pe, const void* weight,
 
 /*
  * As mlaqp_run, but launched with programmatic dependent launch: the kernel
- * may start while the previous kernel on `stream` is still running, streams
+ * may start while earlier kernels on `stream` are still running, streams
  * its weights and scales, reads q_scale, prefetches the q_nope / q_pe lines
  * into L2, and only then waits for the previous kernel to finish before it
  * reads q_nope and q_pe or writes `out`.  It also lets the next kernel on
- * the stream start early.  Use it only when `weight`, `weight_scale` and
- * `q_scale` are not written by the kernel launched immediately before on
- * `stream` (model weights and per-tensor scales written at load time, or by
- * host copies between graph replays, satisfy this).
+ * the stream start early -- for M <= 32 right at its entry -- so in a chain
+ * of such launches more than one earlier kernel can still be running when a
+ * kernel starts.  Use it only when `weight`, `weight_scale` and `q_scale`
+ * are not written by any kernel that may still be running: not by the
+ * preceding programmatic-dependent launches on `stream` back to the last
+ * ordinary launch (model weights and per-tensor scales written at load
+ * time, or by host copies between graph replays, satisfy this).
  */
 int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
                   const void* weight_scale, void* out, int64_t out_row_stride,
@@ -233,8 +236,8 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *   M              0 returns MLAQP_OK without launching; 1..32 supported
  *   H              8, 11 or 16
  *   pdl            != 0: programmatic dependent launch, as mlaqp_run_pdl (the
- *                  weights and scales must not be written by the kernel
- *                  launched just before on `stream`)
+ *                  weights and scales must not be written by any kernel that
+ *                  may still be running, see mlaqp_run_pdl)
  * Status codes as for mlaqp_run.
  */
 #define MLAQP_V_HEAD_DIM 128
