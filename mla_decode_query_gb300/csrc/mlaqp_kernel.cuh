@@ -375,7 +375,11 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // columns n_cta+16w+g / +8, its columns 2t, 2t+1 are tokens.  After
 // movmatrix.trans a lane holds token 8jt+g and columns 16w+2t, +1 (first
 // block) and 16w+8+2t, +1 (second block); stores go straight to
-// out[m*row_stride + h*576 + n].
+// out[m*row_stride + h*576 + n].  BF16: two 4-byte stores per tile.  E4M3:
+// the pairs are 2 bytes each, and 2-byte stores measured far slower than
+// 4-byte ones, so neighbouring lanes (t, t^1) trade one pair: the even lane
+// then holds columns 2t..2t+3, the odd lane 8+2t-2..8+2t+1, and each makes
+// one 4-byte store.
 template <int OD, int MTW, int TS, int MODE>
 __device__ __forceinline__ void write_projection(const RunParams& p, const float (&acc)[MTW][4], int wcol, int wtok,
                                                  int lane, int h, int n_cta, const uint32_t* divtab, float qs,
@@ -398,6 +402,15 @@ __device__ __forceinline__ void write_projection(const RunParams& p, const float
       r[jt][1] = e4m3_pair<MODE>(r[jt][1], divtab, qs, rcp);
     }
   }
+  uint32_t w4[MT];  // E4M3: this lane's 4 contiguous output bytes of tile jt
+  if constexpr (OD == kOutE4M3) {
+#pragma unroll
+    for (int jt = 0; jt < MT; ++jt) {
+      const uint32_t lo = r[jt][0] & 0xFFFFu, hi = r[jt][1] & 0xFFFFu;  // first / second block pair
+      const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, (t & 1) ? lo : hi, 1);
+      w4[jt] = (t & 1) ? (got | (hi << 16)) : (lo | (got << 16));
+    }
+  }
 #pragma unroll
   for (int jt = 0; jt < MT; ++jt) {
     const int m = 8 * (wtok + TS * jt) + g;  // beyond the last tile m >= M: no store
@@ -409,9 +422,8 @@ __device__ __forceinline__ void write_projection(const RunParams& p, const float
         *reinterpret_cast<uint32_t*>(o) = r[jt][0];
         *reinterpret_cast<uint32_t*>(o + 8) = r[jt][1];
       } else {
-        uint8_t* o = p.out + off;
-        *reinterpret_cast<uint16_t*>(o) = static_cast<uint16_t>(r[jt][0]);
-        *reinterpret_cast<uint16_t*>(o + 8) = static_cast<uint16_t>(r[jt][1]);
+        uint8_t* o = p.out + off - 2 * (t & 1) + 8 * (t & 1);  // odd t: columns 8+2(t-1)..
+        *reinterpret_cast<uint32_t*>(o) = w4[jt];
       }
     }
   }
