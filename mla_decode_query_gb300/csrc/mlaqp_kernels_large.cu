@@ -8,7 +8,7 @@ namespace {
 
 template <int K, int TT, int WF, int OD>
 KernelInfo entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, TT>), kLargeThreads,
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, TT>), large_threads(TT),
                     kLargeTilesPerHead, large_smem_layout(K, TT, WF == kWeightMXFP8).bytes};
 }
 

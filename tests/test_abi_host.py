@@ -103,11 +103,13 @@ def test_launch_shape(built_library):
             st, grid, threads = mq.mlaqp_launch_shape(m, h, "mxfp8", "e4m3")
             # one 4-warp token group up to M=8, two groups above
             assert st == mq.MLAQP_OK and grid == 8 * h and threads == (128 if m <= 8 else 256)
-    # above M = 32: the tcgen05 kernel, 4 CTAs of 256 threads per head and
-    # token chunk (32 tokens up to M = 64, 64 up to 128, then 128)
-    for m, chunks in ((33, 2), (64, 2), (65, 2), (128, 2), (129, 2), (200, 2), (256, 2)):
+    # above M = 32: the tcgen05 kernel, 4 CTAs per head and token chunk (32
+    # tokens up to M = 64, 64 up to 128, then 128), 256 threads (512 for the
+    # 64- and 128-token chunks)
+    for m, chunks, thr in ((33, 2, 256), (64, 2, 256), (65, 2, 512), (128, 2, 512), (129, 2, 512),
+                           (200, 2, 512), (256, 2, 512)):
         st, grid, threads = mq.mlaqp_launch_shape(m, 11, "bf16", "bf16")
-        assert st == mq.MLAQP_OK and grid == 4 * 11 * chunks and threads == 256
+        assert st == mq.MLAQP_OK and grid == 4 * 11 * chunks and threads == thr
     assert mq.mlaqp_launch_shape(0, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(257, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(4, 12)[0] == mq.MLAQP_ERR_UNSUPPORTED

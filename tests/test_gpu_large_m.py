@@ -58,7 +58,7 @@ def test_domain_and_launch_shape(cuda_device):
             assert mq.mlaqp_prewarm(h, M_MAX, fmt, od) == mq.MLAQP_OK, mq.mlaqp_last_error()
     assert mq.mlaqp_can_implement(16, M_MAX + 1) == 0
     st, grid, threads = mq.mlaqp_launch_shape(200, 16, "bf16", "bf16")
-    assert st == mq.MLAQP_OK and grid == 4 * 16 * 2 and threads == 256
+    assert st == mq.MLAQP_OK and grid == 4 * 16 * 2 and threads == 512
 
 
 @pytest.mark.parametrize("fmt,od", PAIRS)
