@@ -14,7 +14,7 @@
 // (16 KB BF16) once.  Eight warps split the 512-long contraction, 64 each
 // (four mma.sync m16n8k16 k-steps; swap-AB: the 16 output columns on the
 // MMA's M side, tokens on its N side); the eight partial sums are added in
-// shared memory, rounded to BF16, staged and stored with 16-byte writes.
+// shared memory, rounded to BF16 and stored as 4-byte column pairs.
 //
 // Steps of a CTA (the numbering of the query kernel where it matches):
 //  1. thread 0: two 2-D TMA boxes of 16 columns x 256 rows (+ the head's
@@ -24,7 +24,7 @@
 //  5. the head's x rows into a swizzled smem tile; weight fragments with
 //     ldmatrix.trans;
 //  6. MMAs over this warp's 64 contraction columns;
-//  7. cross-warp sum, BF16 rounding, staged 16-byte stores.
+//  7. cross-warp sum, BF16 rounding, 4-byte stores of column pairs.
 // Every mbarrier wait is bounded as in the query kernel.
 
 #pragma once
@@ -65,8 +65,7 @@ struct VSmem {
   static constexpr int RawBytes = kLatent * kVNTile;
   static constexpr int Scale = Raw + (RedBytes > RawBytes ? RedBytes : RawBytes);  // E8M0 [512][4]
   static constexpr int X = Scale + kLatent * kVScaleRow;   // BF16 [8*MT][512], chunks XOR-swizzled
-  static constexpr int Stage = X + 8 * MT * kLatent * 2;   // BF16 [8*MT][16]
-  static constexpr int Bar = Stage + 8 * MT * kVNTile * 2;
+  static constexpr int Bar = X + 8 * MT * kLatent * 2;
   static constexpr int Bytes = Bar + 64 + 1024;
 };
 
@@ -210,32 +209,32 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
   }
 
   // 7. Cross-warp sum: partial (jt, e, lane) of warp w at red[((w*MT+jt)*4+e)*32+lane].
+  //    D element e of lane ln is output column (ln>>2) + 8*(e>>1) and token
+  //    8jt + 2*(ln&3) + (e&1); lanes ln and ln+4 hold adjacent columns.  Each
+  //    thread below sums one such pair over the 8 warps, rounds it to BF16
+  //    and writes it with one 4-byte store (64*MT pairs).
   float* red = reinterpret_cast<float*>(smem + L::Raw);
 #pragma unroll
   for (int jt = 0; jt < MT; ++jt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) red[((warp * MT + jt) * 4 + e) * 32 + lane] = acc[jt][e];
   __syncthreads();
-  uint16_t* stage = reinterpret_cast<uint16_t*>(smem + L::Stage);
-  for (int t = tid; t < MT * 128; t += kVThreads) {
-    const int jt = t >> 7;
-    const int e = (t >> 5) & 3;
-    const int ln = t & 31;
-    float v = 0.f;
+  if (tid < 64 * MT) {
+    const int t4 = tid & 3;           // lane & 3 of the pair
+    const int gp = (tid >> 2) & 3;    // column pair: lanes 8*gp + t4 and 8*gp + 4 + t4
+    const int e = (tid >> 4) & 3;
+    const int jt = tid >> 6;
+    const int ln = 8 * gp + t4;
+    float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-    for (int w = 0; w < kVWarps; ++w) v += red[((w * MT + jt) * 4 + e) * 32 + ln];
-    // D element e of lane ln: column (ln>>2) + 8*(e>>1), token 8jt + 2*(ln&3) + (e&1).
-    const int col = (ln >> 2) + 8 * (e >> 1);
-    const int tok = 8 * jt + 2 * (ln & 3) + (e & 1);
-    stage[tok * kVNTile + col] = static_cast<uint16_t>(pack_bf16x2(0.f, v));
-  }
-  __syncthreads();
-  // Token row m of the tile: 32 contiguous bytes of the output row.
-  if (tid < 2 * M) {
-    const int m = tid >> 1;
-    const int half = tid & 1;
-    const uint4 v = *reinterpret_cast<const uint4*>(stage + m * kVNTile + 8 * half);
-    *reinterpret_cast<uint4*>(p.out + m * p.out_row_stride + h * kVDim + d_cta + 8 * half) = v;
+    for (int w = 0; w < kVWarps; ++w) {
+      v0 += red[((w * MT + jt) * 4 + e) * 32 + ln];
+      v1 += red[((w * MT + jt) * 4 + e) * 32 + ln + 4];
+    }
+    const int col = 2 * gp + 8 * (e >> 1);   // even: columns col, col+1
+    const int tok = 8 * jt + 2 * t4 + (e & 1);
+    if (tok < M)
+      *reinterpret_cast<uint32_t*>(p.out + tok * p.out_row_stride + h * kVDim + d_cta + col) = pack_bf16x2(v1, v0);
   }
 }
 
