@@ -233,7 +233,8 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *                  out_row_stride >= 128*H and a multiple of 8 elements;
  *                  16-byte aligned; rows >= M and the padding are not written;
  *                  may not overlap an input
- *   M              0 returns MLAQP_OK without launching; 1..32 supported
+ *   M              0 returns MLAQP_OK without launching; 1..256 supported
+ *                  (above 32 the launch covers 32-token chunks, ceil(M/32))
  *   H              8, 11 or 16
  *   pdl            != 0: programmatic dependent launch, as mlaqp_run_pdl (the
  *                  weights and scales must not be written by any kernel that

@@ -188,6 +188,8 @@ LaunchPolicy launch_policy(int weight_format, int out_dtype, int M) {
 }
 
 LaunchPolicy v_up_launch_policy(int weight_format, int M) {
+  if (M > 64) return LaunchPolicy{1, 0};  // 3+ chunks of 32 tokens: more CTAs than one wave (M = 256: 9.4 vs 10.9 us)
+  if (M > 32) return LaunchPolicy{0, 2};  // 2 chunks (M = 33: 3.0 vs 3.8 us)
   if (weight_format == MLAQP_WEIGHT_BF16 && M > 16) return LaunchPolicy{1, 0};
   return LaunchPolicy{0, 2};
 }
@@ -445,8 +447,12 @@ int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
   return MLAQP_OK;
 }
 
+// The V kernel handles 32 tokens per CTA (grid.z chunks above M = 32).
+int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }
+
 const KernelInfo* lookup_v_up(int weight_format, int M, int trig) {
-  return &mlaqp::kernels_v_up()[weight_format][(M + 7) / 8 - 1][trig];
+  const int m = M < mlaqp::kVChunk ? M : mlaqp::kVChunk;
+  return &mlaqp::kernels_v_up()[weight_format][(m + 7) / 8 - 1][trig];
 }
 
 struct VUpArgs {
@@ -465,7 +471,7 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long l
     return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format");
   if (M < 0) return fail(MLAQP_ERR_INVALID_ARG, "M must be >= 0");
   if (!supported_heads(H)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
-  if (M > MLAQP_MAX_M_DECODE) return fail(MLAQP_ERR_UNSUPPORTED, "M must be <= 32 for the V up-projection");
+  if (M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "M must be <= 256");
   if (M == 0) return MLAQP_OK;
   const bool mx = a.weight_format == MLAQP_WEIGHT_MXFP8;
   if (!a.x || !a.weight || !a.out) return fail(MLAQP_ERR_INVALID_ARG, "x, weight and out are required");
@@ -514,7 +520,8 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long l
   params.H = H;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H),
+                     static_cast<unsigned>(v_up_chunks(M)));
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -700,7 +707,7 @@ int mlaqp_v_up_can_implement(int num_heads, int max_m, int weight_format, int de
   if (weight_format != MLAQP_WEIGHT_BF16 && weight_format != MLAQP_WEIGHT_MXFP8)
     return fail(0, "unknown weight_format");
   if (!supported_heads(num_heads)) return fail(0, "num_heads must be 8, 11 or 16");
-  if (max_m < 1 || max_m > MLAQP_MAX_M_DECODE) return fail(0, "max_m must be in 1..32");
+  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(0, "max_m must be in 1..256");
   int dev = 0;
   if (resolve_device(device, &dev) != MLAQP_OK) return 0;
   int count = 0;
@@ -715,7 +722,8 @@ int mlaqp_v_up_prewarm(int num_heads, int max_m, int weight_format, int device) 
   if (weight_format != MLAQP_WEIGHT_BF16 && weight_format != MLAQP_WEIGHT_MXFP8)
     return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format");
   if (!supported_heads(num_heads)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
-  if (max_m < 1 || max_m > MLAQP_MAX_M_DECODE) return fail(MLAQP_ERR_UNSUPPORTED, "max_m must be in 1..32");
+  if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "max_m must be in 1..256");
+  if (max_m > mlaqp::kVChunk) max_m = mlaqp::kVChunk;  // larger M reuses the 32-token kernels
   int dev = 0;
   int st = resolve_device(device, &dev);
   if (st != MLAQP_OK) return st;

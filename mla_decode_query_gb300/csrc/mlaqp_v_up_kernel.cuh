@@ -9,9 +9,10 @@
 // query assembly", section Safety scope); its weight formats follow the
 // query side (section What).
 //
-// Work split: CTA (tile, h) owns head h and output columns [16*tile,
-// 16*tile+16): 8 CTAs per head, each streaming a 512 x 16 weight tile
-// (16 KB BF16) once.  Eight warps split the 512-long contraction, 64 each
+// Work split: CTA (tile, h, z) owns head h, output columns [16*tile,
+// 16*tile+16) and tokens [32z, 32z+32): 8 CTAs per head and 32-token chunk,
+// each streaming a 512 x 16 weight tile (16 KB BF16; later chunks find it
+// in L2).  Eight warps split the 512-long contraction, 64 each
 // (four mma.sync m16n8k16 k-steps; swap-AB: the 16 output columns on the
 // MMA's M side, tokens on its N side); the eight partial sums are added in
 // shared memory, rounded to BF16 and stored as 4-byte column pairs.
@@ -40,6 +41,7 @@ constexpr int kVWarps = 8;
 constexpr int kVThreads = 32 * kVWarps;               // 256
 constexpr int kVKWarp = kLatent / kVWarps;            // 64 contraction columns per warp
 constexpr int kVScaleRow = kVDim / kMxBlock;          // 4 E8M0 bytes per (h, c)
+constexpr int kVChunk = 32;                           // tokens per CTA (grid.z chunks above M = 32)
 
 struct VUpParams {
   CUtensorMap wmap;             // W_UV viewed as [H*512 rows][128 cols], box 16 x 256
@@ -85,9 +87,11 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int M = p.M;
+  const int m0 = blockIdx.z * kVChunk;   // this CTA's tokens: [m0, m0 + M)
+  const int M = min(kVChunk, p.M - m0);   // >= 1: the grid has ceil(M/32) chunks
   const int d_cta = tile * kVNTile;
-  const uint16_t* xh = p.x + h * p.x_hs;
+  const uint16_t* xh = p.x + m0 * p.x_ts + h * p.x_hs;
+  uint16_t* const outc = p.out + m0 * p.out_row_stride;
 
   if constexpr (TRIG == 0) pdl_launch_dependents();
 
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
     const int col = 2 * gp + 8 * (e >> 1);   // even: columns col, col+1
     const int tok = 8 * jt + 2 * t4 + (e & 1);
     if (tok < M)
-      *reinterpret_cast<uint32_t*>(p.out + tok * p.out_row_stride + h * kVDim + d_cta + col) = pack_bf16x2(v1, v0);
+      *reinterpret_cast<uint32_t*>(outc + tok * p.out_row_stride + h * kVDim + d_cta + col) = pack_bf16x2(v1, v0);
   }
 }
 

@@ -169,7 +169,7 @@ def _v_up(**kw):
     (dict(weight_format=3), mq.MLAQP_ERR_INVALID_ARG),
     (dict(M=-1), mq.MLAQP_ERR_INVALID_ARG),
     (dict(H=12), mq.MLAQP_ERR_UNSUPPORTED),
-    (dict(M=33), mq.MLAQP_ERR_UNSUPPORTED),                              # V up-projection: M <= 32
+    (dict(M=257), mq.MLAQP_ERR_UNSUPPORTED),                             # M <= 256
     (dict(x=None), mq.MLAQP_ERR_INVALID_ARG),
     (dict(weight=None), mq.MLAQP_ERR_INVALID_ARG),
     (dict(out=None), mq.MLAQP_ERR_INVALID_ARG),
@@ -191,7 +191,7 @@ def test_v_up_validation(built_library, kw, code):
 
 def test_v_up_zero_tokens_and_domain(built_library):
     assert _v_up(M=0, x=None, out=None) == mq.MLAQP_OK
-    for bad in [dict(num_heads=12), dict(max_m=0), dict(max_m=33), dict(weight_format=4)]:
+    for bad in [dict(num_heads=12), dict(max_m=0), dict(max_m=257), dict(weight_format=4)]:
         a = dict(num_heads=16, max_m=32, weight_format="bf16")
         a.update(bad)
         assert mq.mlaqp_v_up_can_implement(**a) == 0, bad

@@ -52,7 +52,8 @@ def test_domain_and_prewarm(cuda_device):
         for h in (8, 11, 16):
             assert mq.mlaqp_v_up_can_implement(h, 32, fmt) == 1, mq.mlaqp_last_error()
             assert mq.mlaqp_v_up_prewarm(h, 32, fmt) == mq.MLAQP_OK, mq.mlaqp_last_error()
-    assert mq.mlaqp_v_up_can_implement(16, 33) == 0
+    assert mq.mlaqp_v_up_can_implement(16, 256) == 1
+    assert mq.mlaqp_v_up_can_implement(16, 257) == 0
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
@@ -195,3 +196,34 @@ def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device):
         check_bf16_region(_rows(_run(t, M, H, fmt), M, H, V * H), acc, f"after timeout {fmt}")
         st, word = mq.mlaqp_device_status(reset=False)
         assert word == 0
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
+def test_larger_token_counts(cuda_device, fmt):
+    # Above M = 32 the launch covers 32-token chunks (grid z); chunk edges,
+    # ragged tails, strided x and a pitched workspace.
+    H, MM = 11, 256
+    d = inputs.make_v_layer(inputs.layer_seed(57, 0), H, fmt, m_max=MM)
+    _, acc = _oracle(d, fmt)
+    t = _dev(d)
+    for M in (33, 63, 64, 65, 100, 255, 256):
+        got = _rows(_run(t, M, H, fmt, pdl=(M % 2 == 1)), M, H, V * H)
+        check_bf16_region(got, acc[:M], f"v_up {fmt} H{H} M{M}")
+    stride = V * H + 40
+    ws = torch.full((MM * stride + 64,), 0x5A5A, dtype=torch.int16, device="cuda")
+    hm = to_device(np.ascontiguousarray(np.transpose(d["x"], (1, 0, 2))))
+    _run(t, 200, H, fmt, x=hm, x_ts=C, x_hs=MM * C, out=ws, stride=stride)
+    bits = to_host_bits(ws, np.uint16)
+    mask = np.zeros(bits.shape, dtype=bool)
+    for m in range(200):
+        mask[m * stride: m * stride + H * V] = True
+    assert (bits[~mask] == 0x5A5A).all(), "bytes outside the rows changed"
+    check_bf16_region(_rows(ws, 200, H, stride), acc[:200], f"v_up {fmt} M200 head-major pitched")
+
+
+def test_larger_token_counts_bit_exact(cuda_device):
+    for fmt in ("bf16", "mxfp8"):
+        d = inputs.small_integer_v_layer(58, 16, 256, fmt)
+        got = _rows(_run(_dev(d), 256, 16, fmt), 256, 16, V * 16)
+        ref, _ = _oracle(d, fmt)
+        np.testing.assert_array_equal(got, ref, err_msg=f"{fmt} M256")
