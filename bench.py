@@ -191,7 +191,7 @@ class VLayerSet:
         return [self.x[M]]
 
     def kernel_name(self, M):
-        return "mlaqp_v_up_kernel"
+        return "mlaqp_v_up_large_kernel" if M > 64 else "mlaqp_v_up_kernel"
 
     def launch_all(self, M, pdl=True, stream=None):
         import mla_decode_query_gb300 as mq

@@ -234,7 +234,10 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *                  16-byte aligned; rows >= M and the padding are not written;
  *                  may not overlap an input
  *   M              0 returns MLAQP_OK without launching; 1..256 supported
- *                  (above 32 the launch covers 32-token chunks, ceil(M/32))
+ *                  (up to 64: an mma.sync kernel over 32-token chunks; above:
+ *                  a tcgen05 kernel launched in clusters of 4 CTAs, whose
+ *                  tensor memory is taken after the dependency wait and
+ *                  freed before it returns)
  *   H              8, 11 or 16
  *   pdl            != 0: programmatic dependent launch, as mlaqp_run_pdl (the
  *                  weights and scales must not be written by any kernel that

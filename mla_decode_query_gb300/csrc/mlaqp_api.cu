@@ -21,6 +21,7 @@
 #include "mlaqp_kernel.cuh"
 #include "mlaqp_kernel_large.cuh"
 #include "mlaqp_v_up_kernel.cuh"
+#include "mlaqp_v_up_kernel_large.cuh"
 
 namespace {
 
@@ -188,8 +189,7 @@ LaunchPolicy launch_policy(int weight_format, int out_dtype, int M) {
 }
 
 LaunchPolicy v_up_launch_policy(int weight_format, int M) {
-  if (M > 64) return LaunchPolicy{1, 0};  // 3+ chunks of 32 tokens: more CTAs than one wave (M = 256: 9.4 vs 10.9 us)
-  if (M > 32) return LaunchPolicy{0, 2};  // 2 chunks (M = 33: 3.0 vs 3.8 us)
+  if (M > 32) return LaunchPolicy{0, 2};  // two 32-token chunks
   if (weight_format == MLAQP_WEIGHT_BF16 && M > 16) return LaunchPolicy{1, 0};
   return LaunchPolicy{0, 2};
 }
@@ -237,18 +237,24 @@ int large_chunks(int M) {
   return (M + tt - 1) / tt;
 }
 
-// Dynamic shared memory of a large-M launch: the layout's size, padded when
+// Dynamic shared memory for a tcgen05 kernel of `base` bytes whose CTAs
+// hold tmem_cols_for(ntok) TMEM columns each: the layout's size, padded when
 // needed so that the CTAs one SM can hold never ask for more than its 512
-// TMEM columns between them (a CTA of the largest chunk needs
-// tmem_cols_for(chunk) columns).
-int large_smem(const DeviceInfo& d, int base, int M) {
-  const int tt = mlaqp::kLargeTokTiles[large_tile_index(M)];
-  const int chunk = M < tt ? M : tt;
-  const int cols = static_cast<int>(mlaqp::tmem_cols_for((chunk + 15) & ~15));
+// columns between them.
+int tmem_safe_smem(const DeviceInfo& d, int base, int ntok) {
+  const int cols = static_cast<int>(mlaqp::tmem_cols_for(ntok));
   const int max_ctas = 512 / cols;
   if (d.smem_per_sm / (base + d.reserved_per_block) <= max_ctas) return base;
   const int bytes = d.smem_per_sm / (max_ctas + 1) - d.reserved_per_block + 1;
   return bytes < d.max_smem_optin ? bytes : d.max_smem_optin;
+}
+
+// Dynamic shared memory of a large-M launch (a CTA of the largest chunk
+// needs tmem_cols_for(chunk) columns).
+int large_smem(const DeviceInfo& d, int base, int M) {
+  const int tt = mlaqp::kLargeTokTiles[large_tile_index(M)];
+  const int chunk = M < tt ? M : tt;
+  return tmem_safe_smem(d, base, (chunk + 15) & ~15);
 }
 
 int setup_kernels(const DeviceInfo& d) {
@@ -268,6 +274,12 @@ int setup_kernels(const DeviceInfo& d) {
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
           if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
         }
+  for (int wf = 0; wf < 2; ++wf)
+    for (int ti = 0; ti < 2; ++ti) {
+      const cudaError_t e = cudaFuncSetAttribute(mlaqp::kernels_v_up_large()[wf][ti].fn,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
+      if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+    }
   const int smem = policy_max_smem(d);
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
@@ -428,31 +440,49 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
 // V up-projection
 // ---------------------------------------------------------------------------
 
-// 2-D tensor map over W_UV viewed as [H*512 rows][128 columns]; one box is
-// 16 columns x 256 rows (a CTA copies two), unswizzled.
-int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx) {
+// 2-D tensor map over W_UV viewed as [H*512 rows][128 columns].  For the
+// M <= 32 kernel one box is 16 columns x 256 rows, unswizzled (a CTA copies
+// two); for the cluster kernel 64 columns x 128 rows, 128B-swizzled for BF16
+// (the UMMA operand layout) and unswizzled for E4M3 (a CTA copies two).
+int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx, bool large) {
   std::string err;
   EncodeTiledFn fn = encode_tiled_fn(&err);
   if (!fn) return fail(MLAQP_ERR_CUDA, err);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLAQP_V_HEAD_DIM),
                               static_cast<cuuint64_t>(H) * MLAQP_LATENT_DIM};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(MLAQP_V_HEAD_DIM) * (mx ? 1 : 2)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(mlaqp::kVNTile), 256};
+  const cuuint32_t box[2] = {large ? 64u : static_cast<cuuint32_t>(mlaqp::kVNTile),
+                             large ? static_cast<cuuint32_t>(mlaqp::kVLargeK) : 256u};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                         const_cast<void*>(weight), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        large && !mx ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MLAQP_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
   return MLAQP_OK;
 }
 
-// The V kernel handles 32 tokens per CTA (grid.z chunks above M = 32).
+// Up to M = 64 the mma.sync kernel, in 32-token chunks (grid.z); above, the
+// tcgen05 cluster kernel.  Measured on GB300 (H = 16, BF16 W_UV, 128-layer
+// PDL chains, us per layer): the cluster kernel with its trigger after the
+// TMEM allocation takes 3.41 / 3.55 / 4.03 / 5.08 at M = 33 / 64 / 128 /
+// 256, the chunked kernel 3.0 / 3.0 / 5.8 / 9.4.
+constexpr int kVLargeMinM = 65;
+
 int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }
 
 const KernelInfo* lookup_v_up(int weight_format, int M, int trig) {
   const int m = M < mlaqp::kVChunk ? M : mlaqp::kVChunk;
   return &mlaqp::kernels_v_up()[weight_format][(m + 7) / 8 - 1][trig];
+}
+
+// Token tile of the cluster kernel (index into kVLargeTokTiles): 64 up to
+// M = 128, 128 above (M = 256 with 64-token tiles: 5.27 / 6.44 us BF16 /
+// MXFP8, against 5.07 / 5.75).
+int v_large_tile_index(int M) { return M <= 128 ? 0 : 1; }
+
+const KernelInfo* lookup_v_up_large(int weight_format, int M) {
+  return &mlaqp::kernels_v_up_large()[weight_format][v_large_tile_index(M)];
 }
 
 struct VUpArgs {
@@ -502,11 +532,23 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long l
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  const LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
-  const KernelInfo* k = lookup_v_up(a.weight_format, M, pol.trig == 0 ? 0 : 1);
-  const int smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
+  const bool large = M >= kVLargeMinM;
+  const KernelInfo* k = nullptr;
+  int smem_bytes = 0;
+  int chunks = 0;
+  if (large) {
+    k = lookup_v_up_large(a.weight_format, M);
+    const int tt = mlaqp::kVLargeTokTiles[v_large_tile_index(M)];
+    chunks = (M + tt - 1) / tt;
+    smem_bytes = tmem_safe_smem(g_dev[device], k->smem_bytes, ((M < tt ? M : tt) + 15) & ~15);
+  } else {
+    const LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
+    k = lookup_v_up(a.weight_format, M, pol.trig == 0 ? 0 : 1);
+    chunks = v_up_chunks(M);
+    smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
+  }
   mlaqp::VUpParams params;
-  st = encode_v_weight_map(&params.wmap, a.weight, H, mx);
+  st = encode_v_weight_map(&params.wmap, a.weight, H, mx, large);
   if (st != MLAQP_OK) return st;
   params.x = static_cast<const uint16_t*>(a.x);
   params.x_ts = a.x_ts;
@@ -520,18 +562,26 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long l
   params.H = H;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H),
-                     static_cast<unsigned>(v_up_chunks(M)));
+  cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H), static_cast<unsigned>(chunks));
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  if (pdl) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (large) {  // the contraction slices of one (head, chunk) form a cluster
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = static_cast<unsigned>(mlaqp::kVLargeSplit);
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
   }
+  if (pdl) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
+  cfg.attrs = n_attr ? attr : nullptr;
+  cfg.numAttrs = n_attr;
   void* args[1] = {&params};
   const cudaError_t e = cudaLaunchKernelExC(&cfg, k->fn, args);
   if (e != cudaSuccess) return fail_cuda("cudaLaunchKernelExC", e);
@@ -723,7 +773,6 @@ int mlaqp_v_up_prewarm(int num_heads, int max_m, int weight_format, int device) 
     return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format");
   if (!supported_heads(num_heads)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
   if (max_m < 1 || max_m > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "max_m must be in 1..256");
-  if (max_m > mlaqp::kVChunk) max_m = mlaqp::kVChunk;  // larger M reuses the 32-token kernels
   int dev = 0;
   int st = resolve_device(device, &dev);
   if (st != MLAQP_OK) return st;
@@ -735,10 +784,17 @@ int mlaqp_v_up_prewarm(int num_heads, int max_m, int weight_format, int device) 
   if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
   if (prev != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return fail_cuda("cudaSetDevice", e);
   int status = MLAQP_OK;
-  for (int mt = 1; mt <= (max_m + 7) / 8 && status == MLAQP_OK; ++mt)
+  const int chunk_m = max_m < mlaqp::kVChunk ? max_m : mlaqp::kVChunk;
+  for (int mt = 1; mt <= (chunk_m + 7) / 8 && status == MLAQP_OK; ++mt)
     for (int trig = 0; trig < 2 && status == MLAQP_OK; ++trig) {
       cudaFuncAttributes attr;
       e = cudaFuncGetAttributes(&attr, lookup_v_up(weight_format, 8 * mt, trig)->fn);
+      if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
+    }
+  if (max_m >= kVLargeMinM)
+    for (int ti = 0; ti < 2 && status == MLAQP_OK; ++ti) {
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, mlaqp::kernels_v_up_large()[weight_format][ti].fn);
       if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
     }
   if (prev != dev) cudaSetDevice(prev);

@@ -37,6 +37,13 @@ const LargeKernelTable& kernels_large_m();
 using VUpKernelTable = KernelInfo[2][4][2];
 const VUpKernelTable& kernels_v_up();
 
+// V up-projection for 64 < M <= 256 (tcgen05, contraction split over a
+// cluster of tiles_per_head CTAs), [weight_format][token tile] with the
+// token tiles kVLargeTokTiles; grid (tiles_per_head, H, ceil(M / tile)).
+constexpr int kVLargeTokTiles[2] = {64, 128};
+using VUpLargeKernelTable = KernelInfo[2][2];
+const VUpLargeKernelTable& kernels_v_up_large();
+
 // Device status word of each instantiation unit (current device).
 cudaError_t device_status_bf16_weights(unsigned int* value, bool reset);
 cudaError_t device_status_mxfp8_weights(unsigned int* value, bool reset);

@@ -1,7 +1,9 @@
-// Instantiations of the V up-projection kernel: {BF16, MXFP8} W_UV x
-// ceil(M/8) in 1..4 x trigger point {entry, after the wait}.
+// Instantiations of the V up-projection kernels: {BF16, MXFP8} W_UV x
+// ceil(M/8) in 1..4 x trigger point {entry, after the wait} for M <= 64, and
+// {BF16, MXFP8} x token tile {64, 128} of the cluster kernel above M = 64.
 #include "mlaqp_dispatch.h"
 #include "mlaqp_v_up_kernel.cuh"
+#include "mlaqp_v_up_kernel_large.cuh"
 
 namespace mlaqp {
 namespace {
@@ -32,10 +34,32 @@ struct Table {
   }
 };
 
+template <int WF, int TT>
+KernelInfo large_entry() {
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_v_up_large_kernel<WF, TT>), kVLargeThreads, kVLargeSplit,
+                    v_large_smem_layout(TT, WF == kWeightMXFP8).bytes};
+}
+
+struct LargeTable {
+  VUpLargeKernelTable t;
+  LargeTable() {
+    static_assert(kVLargeTokTiles[0] == 64 && kVLargeTokTiles[1] == 128, "token tiles");
+    t[kWeightBF16][0] = large_entry<kWeightBF16, 64>();
+    t[kWeightBF16][1] = large_entry<kWeightBF16, 128>();
+    t[kWeightMXFP8][0] = large_entry<kWeightMXFP8, 64>();
+    t[kWeightMXFP8][1] = large_entry<kWeightMXFP8, 128>();
+  }
+};
+
 }  // namespace
 
 const VUpKernelTable& kernels_v_up() {
   static const Table table;
+  return table.t;
+}
+
+const VUpLargeKernelTable& kernels_v_up_large() {
+  static const LargeTable table;
   return table.t;
 }
 

@@ -9,10 +9,10 @@
 // query assembly", section Safety scope); its weight formats follow the
 // query side (section What).
 //
-// Work split: CTA (tile, h, z) owns head h, output columns [16*tile,
-// 16*tile+16) and tokens [32z, 32z+32): 8 CTAs per head and 32-token chunk,
-// each streaming a 512 x 16 weight tile (16 KB BF16; later chunks find it
-// in L2).  Eight warps split the 512-long contraction, 64 each
+// Used for M <= 64 (above that, mlaqp_v_up_kernel_large.cuh).  Work split:
+// CTA (tile, h, z) owns head h, output columns [16*tile, 16*tile+16) and
+// tokens [32z, 32z+32): 8 CTAs per head and 32-token chunk, each streaming a
+// 512 x 16 weight tile (16 KB BF16; the second chunk finds it in L2).  Eight warps split the 512-long contraction, 64 each
 // (four mma.sync m16n8k16 k-steps; swap-AB: the 16 output columns on the
 // MMA's M side, tokens on its N side); the eight partial sums are added in
 // shared memory, rounded to BF16 and stored as 4-byte column pairs.
@@ -41,10 +41,10 @@ constexpr int kVWarps = 8;
 constexpr int kVThreads = 32 * kVWarps;               // 256
 constexpr int kVKWarp = kLatent / kVWarps;            // 64 contraction columns per warp
 constexpr int kVScaleRow = kVDim / kMxBlock;          // 4 E8M0 bytes per (h, c)
-constexpr int kVChunk = 32;                           // tokens per CTA (grid.z chunks above M = 32)
+constexpr int kVChunk = 32;                           // tokens per CTA (two grid.z chunks for 32 < M <= 64)
 
 struct VUpParams {
-  CUtensorMap wmap;             // W_UV viewed as [H*512 rows][128 cols], box 16 x 256
+  CUtensorMap wmap;             // W_UV viewed as [H*512 rows][128 cols]; box 16 x 256 (64 x 128 for the cluster kernel)
   const uint16_t* x;            // BF16, element (m,h,c) at m*x_ts + h*x_hs + c
   int64_t x_ts, x_hs;           // token / head strides (elements)
   const uint8_t* weight_scale;  // E8M0 [H,512,4] or null

@@ -140,7 +140,7 @@ def test_graph_chain_with_query_projection(cuda_device):
     # A captured PDL chain alternating the query projection and the V
     # up-projection on distinct layers, replayed three times.
     H = 16
-    Ms = (1, 8, 9, 32, 5, 16)
+    Ms = (1, 8, 9, 32, 5, 16, 40, 100, 256, 3)
     steps = []
     for i, M in enumerate(Ms):
         fmt = "bf16" if i % 2 == 0 else "mxfp8"
@@ -177,10 +177,13 @@ def test_graph_chain_with_query_projection(cuda_device):
         np.testing.assert_array_equal(qbits[..., 512:], dq["q_pe"])
 
 
-def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device):
+@pytest.mark.parametrize("M", [4, 100])
+def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device, M):
+    # M = 100 runs the cluster kernel: every CTA gives up on its weight copy
+    # but still passes both cluster barriers, and no cluster writes.
     st, _ = mq.mlaqp_device_status(reset=True)
     assert st == mq.MLAQP_OK
-    H, M = 8, 4
+    H = 8
     for fmt in ("bf16", "mxfp8"):
         d = inputs.make_v_layer(56, H, fmt, m_max=M)
         t = _dev(d)
@@ -199,14 +202,16 @@ def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device):
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
-def test_larger_token_counts(cuda_device, fmt):
-    # Above M = 32 the launch covers 32-token chunks (grid z); chunk edges,
-    # ragged tails, strided x and a pitched workspace.
-    H, MM = 11, 256
-    d = inputs.make_v_layer(inputs.layer_seed(57, 0), H, fmt, m_max=MM)
+@pytest.mark.parametrize("H", [8, 11, 16])
+def test_larger_token_counts(cuda_device, fmt, H):
+    # Above M = 32 the cluster kernel: token tiles of 32 / 64 / 128 and
+    # their edges, ragged tails (16-token MMA padding, chunks of 1 token),
+    # strided x and a pitched workspace.
+    MM = 256
+    d = inputs.make_v_layer(inputs.layer_seed(57, H), H, fmt, m_max=MM)
     _, acc = _oracle(d, fmt)
     t = _dev(d)
-    for M in (33, 63, 64, 65, 100, 255, 256):
+    for M in (33, 47, 63, 64, 65, 100, 128, 129, 200, 255, 256):
         got = _rows(_run(t, M, H, fmt, pdl=(M % 2 == 1)), M, H, V * H)
         check_bf16_region(got, acc[:M], f"v_up {fmt} H{H} M{M}")
     stride = V * H + 40
