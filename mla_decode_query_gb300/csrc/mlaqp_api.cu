@@ -464,9 +464,10 @@ int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx, bo
 
 // Up to M = 64 the mma.sync kernel, in 32-token chunks (grid.z); above, the
 // tcgen05 cluster kernel.  Measured on GB300 (H = 16, BF16 W_UV, 128-layer
-// PDL chains, us per layer): the cluster kernel with its trigger after the
-// TMEM allocation takes 3.41 / 3.55 / 4.03 / 5.08 at M = 33 / 64 / 128 /
-// 256, the chunked kernel 3.0 / 3.0 / 5.8 / 9.4.
+// PDL chains, us per layer): the chunked kernel takes 3.0 / 3.0 / 5.8 / 9.4
+// at M = 33 / 64 / 128 / 256; the cluster kernel 3.23 at M = 65, 3.37 at
+// 128 and 4.80 at 256 (an earlier form of it, 3.41 / 3.55 at M = 33 / 64,
+// never beat the chunked kernel there).
 constexpr int kVLargeMinM = 65;
 
 int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }

@@ -18,25 +18,26 @@
 //     D = FP32 [128 lanes x ntok columns] in TMEM,
 // Token row m of the chunk belongs to CTA m mod 4.  Straight from TMEM, each
 // CTA pushes its partial sums of every row into the owner's receive buffer
-// (distributed shared memory stores, one slot per source CTA), with a status
-// word; one cluster barrier then makes all pushes visible, and each CTA
-// adds the four partials of its own rows from local shared memory in the
-// fixed order kc = 0, 1, 2, 3, rounds to BF16 and stores 8 bytes per thread.
-// No CTA reads another's shared memory and nothing remote is touched after
-// the barrier, so one barrier is all the exchange needs (measured on GB300:
-// a cluster barrier costs ~0.6 us inside a dependent-launch chain, and a
-// pull of the partials through remote loads, behind a second barrier that
-// keeps them alive, cost ~2.3 us per layer at M = 33).
+// (one slot per source CTA) with st.async, which also counts the bytes on
+// the owner's receive mbarrier, and ends with a status word; the owner
+// waits on that barrier alone, then adds the four partials of its rows from
+// local shared memory in the fixed order kc = 0, 1, 2, 3, rounds to BF16 and
+// stores 8 bytes per thread.  The only cluster-wide barrier (every receive
+// mbarrier initialised before any push) is split: arrive at kernel entry,
+// wait just before the first push, so its latency hides behind the weight
+// copy, the dependency wait and the MMAs.  Measured on GB300, a full
+// cluster barrier costs ~0.6 us inside a dependent-launch chain.
 //
 // Every weight byte is read once from HBM (four CTAs per head and chunk,
 // disjoint slices), and x once per chunk; no global scratch is used.
 //
 // Failure handling: every mbarrier wait is bounded.  A CTA that gives up
-// records the timeout, pushes a failure status instead of partials and
-// still arrives at the cluster barrier (there is no early return in this
-// kernel, so no peer can be left waiting); a CTA whose status slots show a
+// records the timeout and still passes the cluster barrier and pushes all
+// its bytes (zeros) with a failure status, so no owner waits for bytes that
+// never come and every CTA stays resident until all bytes meant for it have
+// arrived (there is no early return in this kernel); an owner that sees a
 // failed source writes nothing.  Tensor memory is allocated after
-// griddepcontrol.wait and freed before the cluster barrier.
+// griddepcontrol.wait and freed before the receive wait.
 
 #pragma once
 
@@ -59,7 +60,7 @@ struct VLargeSmem {
   int raw;        // MXFP8 only: E4M3 [2][128][64] as copied (= b)
   int recv;       // FP32 partial sums of this CTA's rows: [4 sources][TT/4 rows][128]
   int scale;      // MXFP8 only: E8M0 [128][4] of the slice
-  int bar;        // two mbarriers: weights, MMA completion
+  int bar;        // three mbarriers: weights, MMA completion, receive
   int tmem_slot;  // TMEM base address written by tcgen05.alloc
   int status;     // [4 sources]: 0 = that source's partials were pushed, 1 = it gave up
   int bytes;      // total, with slack for the 1024-byte alignment
@@ -75,7 +76,7 @@ __host__ __device__ constexpr VLargeSmem v_large_smem_layout(int TT, bool mx) {
   s.recv = s.b + (bx > braw ? bx : braw);
   s.scale = s.recv + TT * kVDim * 4;
   s.bar = s.scale + (mx ? kVLargeK * kVScaleRow : 0);
-  s.tmem_slot = s.bar + 16;
+  s.tmem_slot = s.bar + 32;
   s.status = s.tmem_slot + 16;
   s.bytes = s.status + 16 + 1024;
   return s;
@@ -85,13 +86,6 @@ __host__ __device__ constexpr VLargeSmem v_large_smem_layout(int TT, bool mx) {
 // Cluster helpers (documented PTX only)
 // ---------------------------------------------------------------------------
 
-// All threads of all CTAs of the cluster; release / acquire order this
-// CTA's shared-memory writes before the peers' reads.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Address of the same shared-memory offset in the cluster's CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
   uint32_t r;
@@ -99,8 +93,41 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t ran
   return r;
 }
 
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+// Cluster barrier of all threads of all CTAs, in split form: arrive without
+// ordering anything but the fence issued before it; wait with acquire.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// 4 bytes into a peer's shared memory; completes 4 bytes of the transaction
+// count of the peer's mbarrier `bar` (both cluster addresses of that peer).
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+               "r"(bar)
+               : "memory");
+}
+
+// Bounded wait, with cluster-scope acquire, for a phase that peers complete.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -133,6 +160,10 @@ __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const 
   const uint32_t s_b = smem_u32(smem + L.b);
   const uint32_t bar_w = smem_u32(smem + L.bar);
   const uint32_t bar_mma = bar_w + 8;
+  const uint32_t bar_recv = bar_w + 16;
+  // Bytes pushed into this CTA by its three peers: ntok/4 rows of 128 FP32
+  // values and one status word each.
+  const uint32_t recv_tx = static_cast<uint32_t>(3 * ((ntok / 4) * kVDim * 4 + 4));
   const uint16_t* xs = p.x + m0 * p.x_ts + h * p.x_hs + k0;
 
   // 1. Weight (and scale) stream: two TMA boxes of 64 columns x 128 rows.
@@ -140,7 +171,9 @@ __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const 
     prefetch_tensormap(&p.wmap);
     mbar_init(bar_w, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_recv, 1);
     fence_barrier_init();
+    mbar_arrive_expect_tx(bar_recv, recv_tx);
     const int row = h * kLatent + k0;
     if constexpr (WF == kWeightBF16) {
       mbar_arrive_expect_tx(bar_w, 2 * K * 128 + p.extra_tx);
@@ -158,6 +191,7 @@ __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const 
   // 2. Warm L2 with the chunk's x rows (two 128-byte lines per row slice).
   if (tid < 2 * rows) prefetch_l2(xs + (tid >> 1) * p.x_ts + 64 * (tid & 1));
   __syncthreads();  // barriers initialised before anyone waits on them
+  cluster_arrive_relaxed();  // ... and, once every CTA has arrived, before any peer pushes
 
   // 3. MXFP8: dequantise both 64-column halves into the swizzled BF16 tile
   //    (value = code * 2^(x-127) as two exact power-of-two factors).  Job
@@ -245,8 +279,9 @@ __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const 
   // 8. Wait for the accumulator, then push it: warp w reads TMEM lanes
   //    32*(w%4).. (output column 32*(w%4) + lane), the warp groups take the
   //    16-token column chunks in turn; token t = 16*c16 + i goes to CTA
-  //    t mod 4 = i mod 4, row t/4 of the slot of source kc.  One store
-  //    instruction of a warp writes 128 contiguous bytes of one peer.
+  //    t mod 4 = i mod 4, row t/4 of the slot of source kc (a local store
+  //    when that is this CTA).  One store instruction of a warp writes 128
+  //    contiguous bytes of one peer.  A CTA that gave up pushes zeros.
   if (ok) {
     const bool done = mbar_wait_bounded(bar_mma, 0, p.wait_limit_ns);
     tc_fence_after();
@@ -254,34 +289,58 @@ __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const 
   }
   const uint32_t s_recv = smem_u32(smem + L.recv);
   const uint32_t s_status = smem_u32(smem + L.status);
-  if (ok) {
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
+  uint32_t* status = reinterpret_cast<uint32_t*>(smem + L.status);
+  cluster_wait();  // every peer's receive barrier is initialised
+  {
     const int quarter = warp & 3;
     const int col = 32 * quarter + lane;
-    uint32_t dst[kVLargeSplit];
+    const uint32_t slot = static_cast<uint32_t>((kc * (TT / 4) * kVDim + col) * 4);
+    uint32_t dst[kVLargeSplit], rbar[kVLargeSplit];
 #pragma unroll
-    for (int r = 0; r < kVLargeSplit; ++r) dst[r] = cluster_map(s_recv + static_cast<uint32_t>((kc * (TT / 4) * kVDim + col) * 4), r);
+    for (int r = 0; r < kVLargeSplit; ++r) {
+      dst[r] = cluster_map(s_recv + slot, r);
+      rbar[r] = cluster_map(bar_recv, r);
+    }
     for (int c16 = warp >> 2; c16 < ntok / 16; c16 += kGroups) {
       uint32_t r[16];
-      tmem_ld16(taddr + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(16 * c16), r);
+      if (ok) {
+        tmem_ld16(taddr + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(16 * c16), r);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        st_cluster_u32(dst[i & 3] + static_cast<uint32_t>((4 * c16 + (i >> 2)) * kVDim * 4), r[i]);
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int row = 4 * c16 + (i >> 2);
+        if ((i & 3) == kc) {
+          recv[(kc * (TT / 4) + row) * kVDim + col] = __uint_as_float(r[i]);
+        } else {
+          st_async_u32(dst[i & 3] + static_cast<uint32_t>(row * kVDim * 4), r[i], rbar[i & 3]);
+        }
+      }
     }
   }
-  if (tid < kVLargeSplit) st_cluster_u32(cluster_map(s_status + 4 * kc, tid), ok ? 0u : 1u);
+  if (tid < kVLargeSplit) {
+    if (tid == kc) {
+      status[kc] = ok ? 0u : 1u;
+    } else {
+      st_async_u32(cluster_map(s_status + 4 * kc, tid), ok ? 0u : 1u, cluster_map(bar_recv, tid));
+    }
+  }
   if (tid == 0 && !ok) atomicOr(&g_device_status, kDevStatusWaitTimeout);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(taddr, ncols);
 
-  // 9. One cluster barrier: every push (and status word) is visible.  CTA
-  //    kc then owns token rows m = kc, kc+4, ...; thread item (row j, q)
-  //    adds output columns 4q..4q+3 of the four sources and stores them as
-  //    four BF16 values.
-  cluster_sync();
-  const uint32_t* st = reinterpret_cast<const uint32_t*>(smem + L.status);
-  if ((st[0] | st[1] | st[2] | st[3]) == 0u) {
-    const float* recv = reinterpret_cast<const float*>(smem + L.recv);
+  // 9. Wait for the peers' pushes (the local ones are visible after the CTA
+  //    barrier above).  CTA kc owns token rows m = kc, kc+4, ...; thread item
+  //    (row j, q) adds output columns 4q..4q+3 of the four sources and stores
+  //    them as four BF16 values.
+  const bool got = mbar_wait_bounded_cluster(bar_recv, 0, p.wait_limit_ns);
+  if (__syncthreads_or(!got)) {
+    if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+  } else if ((status[0] | status[1] | status[2] | status[3]) == 0u) {
     for (int i = tid;; i += kVLargeThreads) {
       const int j = i >> 5;
       const int m = kc + kVLargeSplit * j;
