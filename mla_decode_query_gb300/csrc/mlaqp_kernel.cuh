@@ -470,7 +470,6 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   const int lane = tid & 31;
   const int wcol = warp & (kWarps - 1);  // 16-column MMA tile of this warp
   const int wtok = warp / kWarps;        // token group of this warp
-  const int H = p.H;
   const int M = p.M;
   const int n_cta = tile * kNTile;
 
