@@ -15,7 +15,8 @@
 //     A = W_UV rows of the slice, MN-major (output columns contiguous),
 //         128B swizzle: two TMA boxes of 64 columns x 128 rows;
 //     B = the chunk's x rows restricted to the slice, K-major, 128B swizzle;
-//     D = FP32 [128 lanes x ntok columns] in TMEM,
+//     D = FP32 [128 lanes x ntok columns] in TMEM.
+//
 // Token row m of the chunk belongs to CTA m mod 4.  Straight from TMEM, each
 // CTA pushes its partial sums of every row into the owner's receive buffer
 // (one slot per source CTA) with st.async, which also counts the bytes on
@@ -28,8 +29,9 @@
 // copy, the dependency wait and the MMAs.  Measured on GB300, a full
 // cluster barrier costs ~0.6 us inside a dependent-launch chain.
 //
-// Every weight byte is read once from HBM (four CTAs per head and chunk,
-// disjoint slices), and x once per chunk; no global scratch is used.
+// Every weight byte is read once from HBM (the four CTAs of a cluster read
+// disjoint slices; a head's second token chunk finds its slices in L2), and
+// every x byte once; no global scratch is used.
 //
 // Failure handling: every mbarrier wait is bounded.  A CTA that gives up
 // records the timeout and still passes the cluster barrier and pushes all
@@ -108,7 +110,8 @@ __device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t
                : "memory");
 }
 
-// Bounded wait, with cluster-scope acquire, for a phase that peers complete.
+// One test, with cluster-scope acquire, of a barrier phase that peers
+// complete (their st.async writes are visible once it returns true).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -121,6 +124,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Bounded wait for that phase, as mbar_wait_bounded.
 __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
