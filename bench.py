@@ -529,8 +529,9 @@ def run_gpu(args):
             gbs, calls, el = time_oracle(args.cpu_budget, oracle_samples(args.op), op=args.op)
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle_threads(),
                                     "kind": "oracle",
-                                    "sample": f"{calls} oracle layer calls over the 12 (format, M) points, "
-                                              f"{el:.1f} s, layer 0 of each format"}
+                                    "sample": f"{calls} oracle layer calls over 2 formats x M in "
+                                              f"{{{','.join(map(str, M_POINTS))}}} (H={H}), {el:.1f} s, "
+                                              f"layer 0 of each format"}
         print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()
