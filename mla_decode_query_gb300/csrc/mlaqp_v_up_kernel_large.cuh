@@ -341,7 +341,13 @@ __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const 
   //    barrier above).  CTA kc owns token rows m = kc, kc+4, ...; thread item
   //    (row j, q) adds output columns 4q..4q+3 of the four sources and stores
   //    them as four BF16 values.
-  const bool got = mbar_wait_bounded_cluster(bar_recv, 0, p.wait_limit_ns);
+  //    A CTA must not exit while a peer may still push into its shared
+  //    memory.  Before pushing, a peer spends at most two bounded waits
+  //    (weights, MMA commit) of wait_limit_ns each, so the receive wait is
+  //    bounded by three of them plus a quarter: a live peer has always
+  //    pushed (and its bytes have landed) before this CTA gives up.
+  const unsigned long long recv_limit_ns = 3ull * p.wait_limit_ns + (p.wait_limit_ns >> 2);
+  const bool got = mbar_wait_bounded_cluster(bar_recv, 0, recv_limit_ns);
   if (__syncthreads_or(!got)) {
     if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
   } else if ((status[0] | status[1] | status[2] | status[3]) == 0u) {
