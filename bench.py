@@ -80,11 +80,12 @@ class LayerSet:
     and output buffers laid out [L, M, H, *] so each launch reads its own."""
 
     def __init__(self, weight_format, out_dtype, n_layers, h=H, m_points=M_POINTS, device="cuda",
-                 config_index=None, nope=128):
+                 config_index=None, nope=128, arm="auto"):
         import torch
         from mla_decode_query_gb300 import inputs
 
         self.weight_format, self.out_dtype, self.L, self.H, self.K = weight_format, out_dtype, n_layers, h, nope
+        self.arm = arm
         self.m_points = tuple(m_points)
         ci = CONFIG_INDEX[weight_format] if config_index is None else config_index
         m_max = max(32, max(self.m_points))  # the first 32 token rows do not depend on m_max
@@ -118,7 +119,9 @@ class LayerSet:
         return [self.q_nope[M], self.q_pe[M]]
 
     def kernel_name(self, M):
-        return "mlaqp_fused_query_large_kernel" if M > 32 else "mlaqp_fused_query_kernel"
+        if self.arm == "tcgen05" or (self.arm == "auto" and M > 32):
+            return "mlaqp_fused_query_large_kernel"
+        return "mlaqp_fused_query_kernel" if self.arm == "cta_mma" else "mlaqp_query_warp_kernel"
 
     def layer_args(self, M, l):
         return dict(q_nope=self.q_nope[M][l], q_pe=self.q_pe[M][l], weight=self.weight[l],
@@ -128,6 +131,14 @@ class LayerSet:
 
     def launch_all(self, M, pdl=True, stream=None):
         import mla_decode_query_gb300 as mq
+        if self.arm != "auto":  # a forced kernel form (measurement hook)
+            for l in range(self.L):
+                a = self.layer_args(M, l)
+                mq.check(mq.mlaqp_debug_run_arm(a["q_nope"], self.H * self.K, self.K, a["q_pe"], self.H * 64, 64,
+                                                a["weight"], a["weight_scale"], a["out"], a["out_row_stride"],
+                                                a["q_scale"], M, self.H, self.K, self.weight_format, self.out_dtype,
+                                                pdl=pdl, arm=self.arm, stream=stream))
+            return
         if self.K != 128:  # the general entry point: nope dim and (contiguous) strides
             for l in range(self.L):
                 a = self.layer_args(M, l)
@@ -401,6 +412,9 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     mq.load_library()
+    if args.policy:
+        trig, cap = (int(x) for x in args.policy.split(":"))
+        mq.check(mq.mlaqp_debug_set_policy(trig, cap))
 
     m_points = tuple(int(x) for x in args.m.split(",")) if args.m else M_POINTS
     v_up = args.op == "v_up"
@@ -414,7 +428,7 @@ def run_gpu(args):
         for fmt, od in formats:
             L = args.layers or layers_for(fmt, h, v_up)
             sets.append(VLayerSet(fmt, L, h=h, m_points=m_points) if v_up else
-                        LayerSet(fmt, od, L, h=h, m_points=m_points, nope=args.nope))
+                        LayerSet(fmt, od, L, h=h, m_points=m_points, nope=args.nope, arm=args.arm))
 
     def key(s):
         return f"{s.weight_format}->{s.out_dtype}" + (f" H{s.H}" if multi else "")
@@ -512,7 +526,8 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": workload_name(args.nope, m_points, heads, tuple(formats), v_up),
                        "heads": heads[0] if not multi else list(heads), "nope_dim": args.nope,
-                       "m_points": list(m_points),
+                       "m_points": list(m_points), "arm": args.arm,
+                       **({"policy": args.policy} if args.policy else {}),
                        "layers": {key(s): s.L for s in sets}, "pdl": not args.no_pdl,
                        "l2": f"rotated weights per replay {[s.L * s.bytes_per_call(1) >> 20 for s in sets]} MiB "
                              f"vs L2 {L2_BYTES >> 20} MiB (inputs larger than L2, no flush)",
@@ -687,6 +702,10 @@ def main(argv=None):
     ap.add_argument("--heads", type=str, default="16", help="comma-separated head counts (8, 11, 16)")
     ap.add_argument("--op", choices=["query", "v_up"], default="query",
                     help="query: the fused query projection (default); v_up: the V up-projection")
+    ap.add_argument("--arm", choices=["auto", "warp_mma", "warp_fma", "cta_mma", "tcgen05"], default="auto",
+                    help="force one kernel form (measurement; auto = the library's choice)")
+    ap.add_argument("--policy", type=str, default="",
+                    help="trig:cap override of the warp-tile kernel's launch policy (measurement)")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--compare-no-pdl", action="store_true", help="also time the graphs without PDL")
     ap.add_argument("--no-e2e", action="store_true")

@@ -201,6 +201,45 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
                                  unsigned int extra_tx_bytes, mlaqp_stream_t stream);
 
 /*
+ * Measurement hook (no counterpart on the pages): as mlaqp_run_strided, but
+ * the kernel form is forced instead of chosen by the library, so that the
+ * forms can be timed against each other on the same call:
+ *   MLAQP_ARM_AUTO      the library's choice (what mlaqp_run uses)
+ *   MLAQP_ARM_WARP_MMA  warp-tile kernel, mma.sync tensor-core contraction
+ *                       (M <= 32)
+ *   MLAQP_ARM_WARP_FMA  warp-tile kernel, FP32 FMA contraction on the CUDA
+ *                       cores with a warp-shuffle reduction (M <= 8,
+ *                       nope_dim 128)
+ *   MLAQP_ARM_CTA_MMA   the CTA-tile mma.sync kernel (64 latent columns per
+ *                       CTA, q_nope staged in shared memory; M <= 32)
+ *   MLAQP_ARM_TCGEN05   the tcgen05 kernel (TMEM accumulator; any M)
+ * A form that does not cover the call returns MLAQP_ERR_UNSUPPORTED; every
+ * form computes the same result within the projection tolerance, with
+ * identical q_pe columns and E4M3 codes.  Not for production use.
+ */
+#define MLAQP_ARM_AUTO 0
+#define MLAQP_ARM_WARP_MMA 1
+#define MLAQP_ARM_WARP_FMA 2
+#define MLAQP_ARM_CTA_MMA 3
+#define MLAQP_ARM_TCGEN05 4
+int mlaqp_debug_run_arm(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride,
+                        const void* q_pe, int64_t q_pe_token_stride, int64_t q_pe_head_stride,
+                        const void* weight, const void* weight_scale, void* out,
+                        int64_t out_row_stride, const float* q_scale, int M, int H, int nope_dim,
+                        int weight_format, int out_dtype, int pdl, int arm, mlaqp_stream_t stream);
+
+/*
+ * Measurement hook (no counterpart on the pages): overrides, process-wide,
+ * the launch policy of the warp-tile kernel (M <= 32): trig = 0 lets the
+ * next kernel on the stream launch at kernel entry, 1 after the dependency
+ * wait; cta_cap = 1..8 pads shared memory so that at most that many CTAs
+ * share an SM (0: no padding).  trig = -1 restores the library's policy.
+ * Affects launches made after the call (and graphs captured after it).  Not
+ * for production use.  Returns MLAQP_OK or MLAQP_ERR_INVALID_ARG.
+ */
+int mlaqp_debug_set_policy(int trig, int cta_cap);
+
+/*
  * Diagnostic (no counterpart on the pages): launches a kernel of `ctas` x
  * `threads` that does nothing but the programmatic-launch protocol (trigger
  * the next kernel, wait for the previous one), with (pdl != 0) or without

@@ -9,6 +9,7 @@ fails loudly if it has not been built.
 """
 
 from .mlaqp import (  # noqa: F401
+    ARMS,
     MAX_M,
     MAX_M_DECODE,
     V_HEAD_DIM,
@@ -27,6 +28,8 @@ from .mlaqp import (  # noqa: F401
     load_library,
     mlaqp_can_implement,
     mlaqp_debug_launch_null,
+    mlaqp_debug_run_arm,
+    mlaqp_debug_set_policy,
     mlaqp_debug_run_bounded_wait,
     mlaqp_debug_v_up_bounded_wait,
     mlaqp_device_status,

@@ -25,7 +25,7 @@ LIB_DIR = PKG_DIR / "_lib"
 LIB_PATH = LIB_DIR / "libmlaqp.so"
 
 SOURCES = ["mlaqp_api.cu", "mlaqp_kernels_bf16.cu", "mlaqp_kernels_mxfp8.cu", "mlaqp_kernels_large.cu",
-           "mlaqp_kernels_v_up.cu"]
+           "mlaqp_kernels_v_up.cu", "mlaqp_kernels_warp_bf16.cu", "mlaqp_kernels_warp_mxfp8.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -20,6 +20,7 @@
 #include "mlaqp_dispatch.h"
 #include "mlaqp_kernel.cuh"
 #include "mlaqp_kernel_large.cuh"
+#include "mlaqp_kernel_warp.cuh"
 #include "mlaqp_v_up_kernel.cuh"
 #include "mlaqp_v_up_kernel_large.cuh"
 
@@ -57,6 +58,7 @@ struct DeviceInfo {
   int smem_per_sm = 0;        // bytes of shared memory per SM
   int reserved_per_block = 0; // bytes the driver reserves per resident CTA
   int max_smem_optin = 0;     // largest dynamic shared memory a CTA may request
+  int sm_count = 0;           // streaming multiprocessors
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -97,6 +99,7 @@ int check_device(int device) {
       if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
       if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.reserved_per_block, cudaDevAttrReservedSharedMemoryPerBlock, device);
       if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
       if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute", e);
       state = (major == 10 && minor == 3) ? 1 : 2;
       if (state == 1) {
@@ -143,19 +146,24 @@ EncodeTiledFn encode_tiled_fn(std::string* err) {
 }
 
 // 2-D tensor map over W_UK_T viewed as [H*K rows][512 columns]; one box is
-// the K x 64 tile a CTA owns.  BF16 tiles land 128B-swizzled (the layout the
-// kernel's ldmatrix addressing expects); E4M3 tiles land unswizzled.
-int encode_weight_map(CUtensorMap* map, const void* weight, int H, int K, bool mx) {
+// K rows x box_cols columns: the 64-column tile of a CTA of the CTA-tile
+// kernels (BF16 128B-swizzled, the layout their ldmatrix addressing
+// expects; E4M3 unswizzled), or the 16-column tile of a warp of the
+// warp-tile kernel (BF16: 32-byte rows with the 32B swizzle; E4M3:
+// unswizzled 16-byte rows).
+int encode_weight_map(CUtensorMap* map, const void* weight, int H, int K, bool mx, int box_cols, bool swizzle,
+                      bool swizzle32 = false) {
   std::string err;
   EncodeTiledFn fn = encode_tiled_fn(&err);
   if (!fn) return fail(MLAQP_ERR_CUDA, err);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM), static_cast<cuuint64_t>(H) * K};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM) * (mx ? 1 : 2)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(mlaqp::kNTile), static_cast<cuuint32_t>(K)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(K)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                         const_cast<void*>(weight), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        mx ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : (swizzle32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE),
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MLAQP_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
   return MLAQP_OK;
@@ -280,6 +288,25 @@ int setup_kernels(const DeviceInfo& d) {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
       if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
     }
+  for (int wf = 0; wf < 2; ++wf) {
+    const mlaqp::WarpKernelSet& set = wf == 0 ? mlaqp::kernels_warp_bf16_weights() : mlaqp::kernels_warp_mxfp8_weights();
+    for (int ki = 0; ki < 2; ++ki)
+      for (int od = 0; od < 2; ++od)
+        for (int mt = 0; mt < 4; ++mt)
+          for (int trig = 0; trig < 2; ++trig) {
+            const KernelInfo& k = set.mma[ki][od][mt][trig];
+            const cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       smem_for_cap(d, k.smem_bytes, 1));
+            if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+          }
+    for (int od = 0; od < 2; ++od)
+      for (int trig = 0; trig < 2; ++trig) {
+        const KernelInfo& k = set.fma[od][trig];
+        const cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   smem_for_cap(d, k.smem_bytes, 1));
+        if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+      }
+  }
   const int smem = policy_max_smem(d);
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
@@ -333,7 +360,112 @@ RunArgs contiguous_args(const void* q_nope, const void* q_pe, const void* weight
                  weight, weight_scale, out, out_row_stride, q_scale, M, H, MLAQP_NOPE_DIM, weight_format, out_dtype};
 }
 
-int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
+// Which kernel serves a layer call.  kAuto is the library's choice (the
+// warp-tile tensor-core kernel up to M = 32, the tcgen05 kernel above); the
+// others force one form, for measurement (mlaqp_debug_run_arm).
+enum class Arm : int { kAuto = 0, kWarpMma = 1, kWarpFma = 2, kCtaMma = 3, kTcgen05 = 4 };
+
+// The library's kernel choice for a decode call (M <= 32), from 128-layer
+// PDL chains of every M = 1..32, H in {8, 11, 16}, all four format pairs
+// (GB300): the CTA-tile kernel up to the crossover, the warp-tile kernel
+// from it.  Below it the CTA-tile kernel's spare SM slots let the next
+// layer's CTAs start (and stream weights) earlier, which pays while a
+// layer's post-wait work is small; above it the warp-tile kernel's one CTA
+// per SM keeps any SM from carrying two CTAs' contraction and epilogue.
+// Measured crossovers: E4M3 output M = 9 (every H, both weight formats);
+// BF16 -> BF16 M = 9 at H = 8 and 11, 17 at H = 16; MXFP8 -> BF16 M = 13 at
+// H = 8, 17 at H = 11 and 16.  Above 32 tokens: the tcgen05 kernel.
+int warp_crossover(int weight_format, int out_dtype, int H) {
+  if (out_dtype == MLAQP_OUT_E4M3) return 9;
+  if (weight_format == MLAQP_WEIGHT_BF16) return H <= 11 ? 9 : 17;
+  return H <= 8 ? 13 : 17;
+}
+
+Arm auto_arm(int weight_format, int out_dtype, int M, int H) {
+  if (M > MLAQP_MAX_M_DECODE) return Arm::kTcgen05;
+  return M >= warp_crossover(weight_format, out_dtype, H) ? Arm::kWarpMma : Arm::kCtaMma;
+}
+
+// Grid of a warp-tile launch: one CTA per SM, but at least 8 CTAs per head
+// (at most kWMaxTilesPerCta tiles per CTA) and at most 32 (one tile each);
+// the kernel splits the CTAs over the heads as evenly as it goes.
+void warp_grid(const DeviceInfo& d, int H, int* ctas, int* tiles_per_cta) {
+  const int min_g = H * ((mlaqp::kWTilesPerHead + mlaqp::kWMaxTilesPerCta - 1) / mlaqp::kWMaxTilesPerCta);
+  const int max_g = H * mlaqp::kWTilesPerHead;
+  const int g = d.sm_count < min_g ? min_g : (d.sm_count > max_g ? max_g : d.sm_count);
+  *ctas = g;
+  *tiles_per_cta = (mlaqp::kWTilesPerHead + g / H - 1) / (g / H);  // the fewest CTAs a head gets is g / H
+}
+
+const KernelInfo* lookup_warp(int weight_format, int out_dtype, int M, int trig, int nope_idx, bool fma) {
+  const mlaqp::WarpKernelSet& set =
+      weight_format == MLAQP_WEIGHT_BF16 ? mlaqp::kernels_warp_bf16_weights() : mlaqp::kernels_warp_mxfp8_weights();
+  if (fma) return &set.fma[out_dtype][trig];
+  return &set.mma[nope_idx][out_dtype][(M + 7) / 8 - 1][trig];
+}
+
+// Measurement override of the warp-tile launch policy (mlaqp_debug_set_policy):
+// trig < 0 means none.
+std::atomic<int> g_policy_trig{-1};
+std::atomic<int> g_policy_cap{0};
+
+// Launch policy of the warp-tile kernel: trigger at entry, at most 2 CTAs per
+// SM (with one CTA per SM per launch, a running layer and the next one each
+// hold one slot of every SM).
+LaunchPolicy warp_launch_policy(int /*weight_format*/, int /*out_dtype*/, int /*M*/) {
+  const int trig = g_policy_trig.load(std::memory_order_relaxed);
+  if (trig >= 0) return LaunchPolicy{trig, g_policy_cap.load(std::memory_order_relaxed)};
+  return LaunchPolicy{0, 2};
+}
+
+int launch_warp(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx,
+                Arm arm, int device) {
+  const int M = a.M, H = a.H, K = a.K;
+  const bool mx = a.weight_format == MLAQP_WEIGHT_MXFP8;
+  const LaunchPolicy pol = warp_launch_policy(a.weight_format, a.out_dtype, M);
+  const KernelInfo* k = lookup_warp(a.weight_format, a.out_dtype, M, pol.trig, nope_index(K), arm == Arm::kWarpFma);
+  int ctas = 0, tpc = 0;
+  warp_grid(g_dev[device], H, &ctas, &tpc);
+  mlaqp::WarpRunParams params;
+  int st = encode_weight_map(&params.wmap, a.weight, H, K, mx, mlaqp::kWTileCols, false, !mx);
+  if (st != MLAQP_OK) return st;
+  params.q_nope = static_cast<const uint16_t*>(a.q_nope);
+  params.q_pe = static_cast<const uint16_t*>(a.q_pe);
+  params.q_nope_ts = a.q_nope_ts;
+  params.q_nope_hs = a.q_nope_hs;
+  params.q_pe_ts = a.q_pe_ts;
+  params.q_pe_hs = a.q_pe_hs;
+  params.weight_scale = static_cast<const uint8_t*>(a.weight_scale);
+  params.out = static_cast<uint8_t*>(a.out);
+  params.out_row_stride = a.out_row_stride;
+  params.q_scale = a.q_scale;
+  params.wait_limit_ns = wait_limit_ns;
+  params.extra_tx = extra_tx;
+  params.M = M;
+  params.H = H;
+  params.inv_ctas = 1.0f / static_cast<float>(ctas);
+  params.inv_heads = 1.0f / static_cast<float>(H);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(k->threads * tpc), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0));
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {&params};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, k->fn, args);
+  if (e != cudaSuccess) return fail_cuda("cudaLaunchKernelExC", e);
+  return MLAQP_OK;
+}
+
+int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx,
+             Arm forced = Arm::kAuto) {
   const int M = a.M, H = a.H, K = a.K;
   if (!valid_enums(a.weight_format, a.out_dtype)) return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format or out_dtype");
   if (M < 0) return fail(MLAQP_ERR_INVALID_ARG, "M must be >= 0");
@@ -388,7 +520,15 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  const bool large = M > MLAQP_MAX_M_DECODE;
+  Arm arm = forced;
+  if (arm == Arm::kAuto) arm = auto_arm(a.weight_format, a.out_dtype, M, H);
+  if (arm == Arm::kWarpFma && (M > 8 || K != 128))
+    return fail(MLAQP_ERR_UNSUPPORTED, "the CUDA-core arm covers M <= 8 at nope_dim 128");
+  if ((arm == Arm::kWarpMma || arm == Arm::kCtaMma) && M > MLAQP_MAX_M_DECODE)
+    return fail(MLAQP_ERR_UNSUPPORTED, "the mma.sync arms cover M <= 32");
+  if (arm == Arm::kWarpMma || arm == Arm::kWarpFma) return launch_warp(a, stream, pdl, wait_limit_ns, extra_tx, arm, device);
+
+  const bool large = arm == Arm::kTcgen05;
   const KernelInfo* k = nullptr;
   int smem_bytes = 0;
   if (large) {
@@ -400,7 +540,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
     smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   }
   RunParams params;
-  st = encode_weight_map(&params.wmap, a.weight, H, K, mx);
+  st = encode_weight_map(&params.wmap, a.weight, H, K, mx, mlaqp::kNTile, !mx);
   if (st != MLAQP_OK) return st;
   params.q_nope = static_cast<const uint16_t*>(a.q_nope);
   params.q_pe = static_cast<const uint16_t*>(a.q_pe);
@@ -630,13 +770,21 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
   for (int mt = 1; mt <= (decode_m + 7) / 8 && status == MLAQP_OK; ++mt) {
     const uint32_t bit = 1u << (((weight_format * 2 + out_dtype) * 4) + (mt - 1));
     if (g_prewarmed[dev].load(std::memory_order_acquire) & bit) continue;
-    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)
+    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki) {
       for (int trig = 0; trig < mlaqp::kTrigVariants && status == MLAQP_OK; ++trig) {
         const KernelInfo* k = lookup(weight_format, out_dtype, 8 * mt, trig, ki);
         cudaFuncAttributes attr;
         e = cudaFuncGetAttributes(&attr, k->fn);  // forces the kernel image to load
         if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
       }
+      for (int trig = 0; trig < 2 && status == MLAQP_OK; ++trig) {
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, lookup_warp(weight_format, out_dtype, 8 * mt, trig, ki, false)->fn);
+        if (e == cudaSuccess && mt == 1 && ki == 0)
+          e = cudaFuncGetAttributes(&attr, lookup_warp(weight_format, out_dtype, 8, trig, 0, true)->fn);
+        if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
+      }
+    }
     if (status != MLAQP_OK) break;
     g_prewarmed[dev].fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -688,9 +836,22 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
     if (threads_per_cta) *threads_per_cta = k->threads;
     return MLAQP_OK;
   }
-  const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0);
-  if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
-  if (threads_per_cta) *threads_per_cta = k->threads;
+  if (auto_arm(weight_format, out_dtype, M, H) == Arm::kCtaMma) {
+    const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0);
+    if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
+    if (threads_per_cta) *threads_per_cta = k->threads;
+    return MLAQP_OK;
+  }
+  int dev = 0;
+  int st = resolve_device(-1, &dev);
+  if (st != MLAQP_OK) return st;
+  st = check_device(dev);
+  if (st != MLAQP_OK) return st;
+  const KernelInfo* k = lookup_warp(weight_format, out_dtype, M, 0, 0, false);
+  int ctas = 0, tpc = 0;
+  warp_grid(g_dev[dev], H, &ctas, &tpc);
+  if (grid_ctas) *grid_ctas = ctas;
+  if (threads_per_cta) *threads_per_cta = k->threads * tpc;
   return MLAQP_OK;
 }
 
@@ -705,15 +866,36 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
                   stream, false, wait_limit_ns, extra_tx_bytes);
 }
 
+int mlaqp_debug_run_arm(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride, const void* q_pe,
+                        int64_t q_pe_token_stride, int64_t q_pe_head_stride, const void* weight,
+                        const void* weight_scale, void* out, int64_t out_row_stride, const float* q_scale, int M,
+                        int H, int nope_dim, int weight_format, int out_dtype, int pdl, int arm,
+                        mlaqp_stream_t stream) {
+  if (arm < 0 || arm > 4) return fail(MLAQP_ERR_INVALID_ARG, "arm must be in 0..4");
+  const RunArgs a{q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_pe_token_stride, q_pe_head_stride,
+                  weight, weight_scale, out, out_row_stride, q_scale, M, H, nope_dim, weight_format, out_dtype};
+  return run_impl(a, stream, pdl != 0, kDefaultWaitLimitNs, 0, static_cast<Arm>(arm));
+}
+
+int mlaqp_debug_set_policy(int trig, int cta_cap) {
+  if (trig < -1 || trig > 1 || cta_cap < 0 || cta_cap > 8)
+    return fail(MLAQP_ERR_INVALID_ARG, "trig must be -1, 0 or 1 and cta_cap in 0..8");
+  g_policy_cap.store(cta_cap, std::memory_order_relaxed);
+  g_policy_trig.store(trig, std::memory_order_relaxed);
+  return MLAQP_OK;
+}
+
 int mlaqp_device_status(unsigned int* status, int reset) {
   if (!status) return fail(MLAQP_ERR_INVALID_ARG, "status must not be NULL");
-  unsigned int a = 0, b = 0, c = 0, v = 0;
+  unsigned int a = 0, b = 0, c = 0, v = 0, wa = 0, wb = 0;
   cudaError_t e = mlaqp::device_status_bf16_weights(&a, reset != 0);
   if (e == cudaSuccess) e = mlaqp::device_status_mxfp8_weights(&b, reset != 0);
   if (e == cudaSuccess) e = mlaqp::device_status_large_m(&c, reset != 0);
   if (e == cudaSuccess) e = mlaqp::device_status_v_up(&v, reset != 0);
+  if (e == cudaSuccess) e = mlaqp::device_status_warp_bf16(&wa, reset != 0);
+  if (e == cudaSuccess) e = mlaqp::device_status_warp_mxfp8(&wb, reset != 0);
   if (e != cudaSuccess) return fail_cuda("reading the device status word", e);
-  *status = a | b | c | v;
+  *status = a | b | c | v | wa | wb;
   return MLAQP_OK;
 }
 

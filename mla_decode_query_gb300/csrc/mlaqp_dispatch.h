@@ -24,6 +24,18 @@ using KernelTable = KernelInfo[2][2][4][kTrigVariants];
 const KernelTable& kernels_bf16_weights();
 const KernelTable& kernels_mxfp8_weights();
 
+// Warp-tile query kernels (M <= 32), per weight format: the tensor-core
+// arm [nope][out_dtype][mt-1][trig] and the CUDA-core arm [out_dtype][trig]
+// (M <= 8, nope 128); trig 0: at entry, 1: after the dependency wait.
+// threads = 32 x token groups per tile slot (the launch multiplies it by the
+// tile slots of a CTA); smem_bytes = the unpadded layout size.
+struct WarpKernelSet {
+  KernelInfo mma[2][2][4][2];
+  KernelInfo fma[2][2];
+};
+const WarpKernelSet& kernels_warp_bf16_weights();
+const WarpKernelSet& kernels_warp_mxfp8_weights();
+
 // tcgen05 kernels for 32 < M <= 256, [nope][token tile][weight_format][out_dtype]
 // with token tiles kLargeTokTiles (tokens per CTA); the grid is
 // (tiles_per_head, H, ceil(M / token tile)) and smem_bytes the unpadded
@@ -49,5 +61,7 @@ cudaError_t device_status_bf16_weights(unsigned int* value, bool reset);
 cudaError_t device_status_mxfp8_weights(unsigned int* value, bool reset);
 cudaError_t device_status_large_m(unsigned int* value, bool reset);
 cudaError_t device_status_v_up(unsigned int* value, bool reset);
+cudaError_t device_status_warp_bf16(unsigned int* value, bool reset);
+cudaError_t device_status_warp_mxfp8(unsigned int* value, bool reset);
 
 }  // namespace mlaqp

@@ -58,6 +58,10 @@ _SIGNATURES = {
     "mlaqp_run_strided": (_c_int, [_c_void_p, ctypes.c_int64, ctypes.c_int64, _c_void_p, ctypes.c_int64,
                                    ctypes.c_int64, _c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, _c_void_p,
                                    _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
+    "mlaqp_debug_run_arm": (_c_int, [_c_void_p, ctypes.c_int64, ctypes.c_int64, _c_void_p, ctypes.c_int64,
+                                     ctypes.c_int64, _c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, _c_void_p,
+                                     _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
+    "mlaqp_debug_set_policy": (_c_int, [_c_int, _c_int]),
     "mlaqp_launch_shape": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_int),
                                     ctypes.POINTER(_c_int)]),
     "mlaqp_device_status": (_c_int, [ctypes.POINTER(ctypes.c_uint), _c_int]),
@@ -171,6 +175,23 @@ def mlaqp_run_strided(q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_p
         int(q_pe_head_stride), _ptr(weight), _ptr(weight_scale), _ptr(out), int(out_row_stride), _ptr(q_scale),
         int(M), int(H), int(nope_dim), _fmt(weight_format, WEIGHT_FORMATS), _fmt(out_dtype, OUT_DTYPES),
         1 if pdl else 0, _stream(stream))
+
+
+ARMS = {"auto": 0, "warp_mma": 1, "warp_fma": 2, "cta_mma": 3, "tcgen05": 4}
+
+
+def mlaqp_debug_run_arm(q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_pe_token_stride, q_pe_head_stride,
+                        weight, weight_scale, out, out_row_stride, q_scale, M, H, nope_dim, weight_format, out_dtype,
+                        pdl=False, arm="auto", stream=None) -> int:
+    return load_library().mlaqp_debug_run_arm(
+        _ptr(q_nope), int(q_nope_token_stride), int(q_nope_head_stride), _ptr(q_pe), int(q_pe_token_stride),
+        int(q_pe_head_stride), _ptr(weight), _ptr(weight_scale), _ptr(out), int(out_row_stride), _ptr(q_scale),
+        int(M), int(H), int(nope_dim), _fmt(weight_format, WEIGHT_FORMATS), _fmt(out_dtype, OUT_DTYPES),
+        1 if pdl else 0, _fmt(arm, ARMS), _stream(stream))
+
+
+def mlaqp_debug_set_policy(trig, cta_cap) -> int:
+    return load_library().mlaqp_debug_set_policy(int(trig), int(cta_cap))
 
 
 def mlaqp_debug_run_bounded_wait(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H,

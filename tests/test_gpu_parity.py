@@ -25,11 +25,17 @@ def _dev_layer(d, dev):
                 weight_scale=None if d["weight_scale"] is None else to_device(d["weight_scale"], dev))
 
 
-def _run(t, M, H, fmt, od, q_scale=None, out=None, stride=None, pdl=False, dev="cuda"):
+def _run(t, M, H, fmt, od, q_scale=None, out=None, stride=None, pdl=False, dev="cuda", arm="auto"):
     stride = stride or D * H
     if out is None:
         out = torch.zeros((M * stride,), dtype=torch.int16 if od == "bf16" else torch.uint8, device=dev)
     qs = None if q_scale is None else torch.tensor([q_scale], dtype=torch.float32, device=dev)
+    if arm != "auto":
+        st = mq.mlaqp_debug_run_arm(t["q_nope"], H * 128, 128, t["q_pe"], H * 64, 64, t["weight"], t["weight_scale"],
+                                    out, stride, qs, M, H, 128, fmt, od, pdl=pdl, arm=arm)
+        assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
+        torch.cuda.synchronize()
+        return out
     fn = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
     st = fn(t["q_nope"], t["q_pe"], t["weight"], t["weight_scale"], out, stride, qs, M, H, fmt, od)
     assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
@@ -184,15 +190,21 @@ def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device):
         assert word == 0
 
 
-@pytest.mark.parametrize("M", [8, 32, 64])
-@pytest.mark.parametrize("qs", [0.01, 0.0371, 0.1, 3.0, 1e-20, 1e20, 2.0 ** -110, 2.0 ** 110])
-def test_e4m3_division_every_bf16_value(cuda_device, qs, M):
+@pytest.mark.parametrize("M,arm", [(8, "auto"), (32, "auto"), (64, "auto"), (8, "cta_mma"), (32, "cta_mma"),
+                                   (4, "warp_fma")])
+@pytest.mark.parametrize("qs", [0.01, 0.0371, 0.1, 3.0, 1e-20, 1e20, 2.0 ** -110, 2.0 ** 110,
+                                0.012109374627470970, 0.02734375])
+def test_e4m3_division_every_bf16_value(cuda_device, qs, M, arm):
     # The q_pe columns of an E4M3 output are e4m3_satfinite(q_pe / q_scale):
     # feed every non-NaN BF16 bit pattern through them and require the codes
-    # bit for bit.  The scales cover the kernels' exact table and multiply
-    # paths (M = 8: decode kernel, table; M = 32: decode kernel, multiply;
-    # M = 64: tcgen05 kernel, multiply), results that overflow or underflow
-    # binary32, and q_scale outside 2^-100..2^100 (plain division).
+    # bit for bit.  The scales cover every exact conversion form: the
+    # warp-tile kernels' one-multiply form (M = 8, 32, 4: allowed by the
+    # per-CTA check for most scales) and their table fallback (the last two
+    # scales, for which the check refuses: one multiply by RN(1/q_scale)
+    # would get 32 and 60 BF16 values' codes wrong); the CTA-tile kernel's
+    # table (M = 8) and checked-multiply (M = 32) forms; the tcgen05 kernel
+    # (M = 64); results that overflow or underflow binary32; and q_scale
+    # outside 2^-100..2^100 (plain division).
     H = 16
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # drop inf / NaN patterns
@@ -205,7 +217,7 @@ def test_e4m3_division_every_bf16_value(cuda_device, qs, M):
         pe[:chunk.size] = chunk
         pe = pe.reshape(M, H, 64)
         dd = dict(d, q_pe=pe)
-        got = _rows(_run(_dev_layer(dd, "cuda"), M, H, "bf16", "e4m3", qs), M, H, D * H, "e4m3")
+        got = _rows(_run(_dev_layer(dd, "cuda"), M, H, "bf16", "e4m3", qs, arm=arm), M, H, D * H, "e4m3")
         with np.errstate(all="ignore"):
             ref = oracle.f32_to_e4m3_satfinite(oracle.bf16_to_f32(pe) / qs)
         np.testing.assert_array_equal(got[..., 512:], ref, err_msg=f"q_scale={qs} chunk {start}")
