@@ -18,13 +18,16 @@
 //  2. warp 0 warms L2 with the head's q_nope / q_pe rows (prefetch only);
 //     q_scale is read (a per-tensor constant, like the weights);
 //  3. MXFP8: all threads wait for the copy and dequantise into the same
-//     swizzled BF16 tile (e4m3 * 2^(e8m0-127), exact); E4M3 output: each
-//     thread adds one entry to the exact division table (see div_by_table);
+//     swizzled BF16 tile (e4m3 * 2^(e8m0-127), exact); BF16: all threads
+//     wait for the copy and load their weight fragments (ldmatrix.trans);
+//     E4M3 output: each of 128 threads adds one entry to the exact
+//     division table and checks one significand for the exact one-multiply
+//     conversion (see e4m3_mul_exact_for);
 //  4. griddepcontrol.wait -- everything above is independent of the
 //     previous kernel, so under programmatic dependent launch it overlaps
 //     that kernel; everything below reads inputs it may have produced;
 //  5. q_nope rows into a swizzled smem tile (16-byte loads), q_pe pairs into
-//     registers, the weight fragments with ldmatrix.trans;
+//     registers, the MXFP8 weight fragments with ldmatrix.trans;
 //  8. q_pe appended (bit copy or E4M3 cast), one value pair per thread,
 //     ahead of the contraction so that it overlaps the MMA latency;
 //  6. mma.sync m16n8k16 BF16 -> FP32 with the latent axis on the MMA's M
@@ -311,44 +314,56 @@ static __device__ __noinline__ uint32_t e4m3_pair_divide(uint32_t two_bf16, floa
   return pack_e4m3x2(__fdiv_rn(bf16_hi(two_bf16), qs), __fdiv_rn(bf16_lo(two_bf16), qs));
 }
 
-// Table form of the exact conversion below (kept out of line: it serves the
-// rare values the multiply cannot decide).
-static __device__ __noinline__ uint32_t e4m3_pair_table(uint32_t two_bf16, const uint32_t* tab) {
-  return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
-}
-
-// True when y = RN(a * RN(1/q_scale)) converts to the same E4M3 code as the
-// IEEE quotient RN(a / q_scale).  With r = RN(1/q_scale) = (1/q_scale)(1+d),
-// |d| <= 2^-24, y = (a/q_scale)(1+d)(1+e), |e| <= 2^-24, so y and RN(a/q_scale)
-// are at most 3 binary32 ulps (of y) apart.  The RNE conversion to E4M3 of a
-// value of magnitude >= 2^-6 (the E4M3 normal range; above 448 both saturate)
-// keeps 3 mantissa bits, so its result changes only across a midpoint, a value
-// whose low 20 mantissa bits are 0x80000.  y qualifies if |y| >= 2^-6 and its
-// low 20 bits are more than 8 from 0x80000; NaN, zero, tiny and near-midpoint
-// values do not, and take the table path.
-__device__ __forceinline__ bool e4m3_mul_decides(float y) {
-  const uint32_t low = __float_as_uint(y) & 0xFFFFFu;
-  return fabsf(y) >= 0x1p-6f && (low - (0x80000u - 8u)) > 16u;
+// True when one multiply by rcp = RN(1/q_scale) gives, for every BF16 value
+// p, the E4M3 code of the IEEE quotient RN(p / q_scale); one thread checks
+// one significand 128 + f, and a CTA takes the AND over f = 0..127.
+//
+// Why it suffices.  A normal BF16 value is p = (128 + f) * 2^j.  While the
+// results stay normal binary32 values, RN(p * rcp) = RN((128+f) * rcp) * 2^j
+// = m * 2^j and RN(p / q) = t * 2^j with t = RN((128+f) / q), because
+// rounding commutes with scaling by a power of two.  The E4M3 code of x * 2^j
+// depends on j only through the regime x * 2^j falls in: at or above 2^-6
+// (E4M3 normals and saturation) the code is the same 3-bit rounding of the
+// significand for every j, in [2^-10, 2^-6) the rounding step is 2^-9, and
+// below 2^-10 everything rounds to zero.  m and t are at most a few binary32
+// ulps apart, so comparing the codes of m * 2^k and t * 2^k with k chosen to
+// put t into each binade 2^-11 .. 2^-7 and into [1, 2) covers every j.
+// Values outside the normal range decide the same code either way (zero,
+// BF16 subnormals, infinities: +-0 or +-448) given 2^-100 <= q <= 2^100,
+// which the caller checks.  A refusal only costs speed: the CTA then uses
+// the division table.
+__device__ __forceinline__ bool e4m3_mul_exact_for(int f, float qs, float rcp) {
+  const float num = static_cast<float>(128 + f);
+  const float t = __fdiv_rn(num, qs);
+  const float m = __fmul_rn(num, rcp);
+  const int et = static_cast<int>((__float_as_uint(t) >> 23) & 0xFFu) - 127;
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < 6; ++i) {
+    const int target = i < 5 ? -11 + i : 0;
+    const float s = __uint_as_float(static_cast<uint32_t>(target - et + 127) << 23);  // 2^(target - et)
+    const uint32_t codes = pack_e4m3x2(__fmul_rn(t, s), __fmul_rn(m, s));
+    ok = ok && ((codes & 0xFFu) == (codes >> 8));
+  }
+  return ok;
 }
 
 // How a kernel converts value / q_scale to E4M3 (all three give the code of
-// the IEEE binary32 quotient, saturating RNE):
-//   kE4m3Divide: plain IEEE division (q_scale outside [2^-100, 2^100]);
-//   kE4m3Table:  the division table (div_by_table), no branch;
-//   kE4m3Mul:    one multiply by rcp = RN(1/q_scale), exact whenever
-//                e4m3_mul_decides holds, else the table (fewer instructions
-//                per value; the decode kernel keeps the table at M <= 8,
-//                where measurement favours it).
-enum E4m3Mode : int { kE4m3Divide = 0, kE4m3Table = 1, kE4m3Mul = 2 };
+// the IEEE binary32 quotient, saturating RNE), chosen once per CTA:
+//   kE4m3Divide:   plain IEEE division (q_scale outside [2^-100, 2^100]);
+//   kE4m3Table:    the division table (div_by_table), when the check below
+//                  refuses the multiply;
+//   kE4m3MulExact: one multiply by rcp = RN(1/q_scale), when
+//                  e4m3_mul_exact_for held for every significand (almost
+//                  every scale: 800 of 800 random ones in [2^-99, 2^99] and
+//                  [0.01, 0.1] in a CPU check).
+enum E4m3Mode : int { kE4m3Divide = 0, kE4m3Table = 1, kE4m3MulExact = 3 };
 
 // Two BF16 values (packed) -> two E4M3 codes (packed, low value in byte 0).
 template <int MODE>
 __device__ __forceinline__ uint32_t e4m3_pair(uint32_t two_bf16, const uint32_t* tab, float qs, float rcp) {
-  if constexpr (MODE == kE4m3Mul) {
-    const float hi = __fmul_rn(bf16_hi(two_bf16), rcp);
-    const float lo = __fmul_rn(bf16_lo(two_bf16), rcp);
-    if (e4m3_mul_decides(hi) && e4m3_mul_decides(lo)) return pack_e4m3x2(hi, lo);
-    return e4m3_pair_table(two_bf16, tab);
+  if constexpr (MODE == kE4m3MulExact) {
+    return pack_e4m3x2(__fmul_rn(bf16_hi(two_bf16), rcp), __fmul_rn(bf16_lo(two_bf16), rcp));
   } else if constexpr (MODE == kE4m3Table) {
     return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
   } else {
@@ -457,7 +472,6 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   constexpr int MTW = (MT + TS - 1) / TS;   // token tiles per warp
   constexpr int KS = K / 16;                // MMA k-steps
   constexpr int KC = K / 8;                 // 16-byte chunks per q_nope row
-  constexpr int kTableMode = MT >= 2 ? kE4m3Mul : kE4m3Table;  // E4M3 conversion with the table available
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s_a = smem_u32(smem + L::A);
@@ -563,15 +577,42 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     pdl_launch_dependents();
   }
 
-  // E4M3 output: table of RN((128+f)/q_scale), one entry per thread, made
-  // visible by the barrier after the q_nope tile is stored.
+  // E4M3 output: table of RN((128+f)/q_scale) and the per-significand check
+  // of the one-multiply form, one significand per thread (both uniform
+  // across the grid: q_scale is one value).
   uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L::Div);
-  bool table_ok = false;
+  bool table_ok = false, mul_ok = false;
   float rcp = 1.f;
   if constexpr (OD == kOutE4M3) {
-    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
-    if (table_ok && tid < 128) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;
     rcp = __frcp_rn(qs);
+    bool mine = table_ok;
+    if (table_ok && tid < 128) {
+      divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+      mine = e4m3_mul_exact_for(tid, qs, rcp);
+    }
+    mul_ok = __syncthreads_and(mine);  // also publishes the table
+  }
+
+  // A fragments (weights, transposed by ldmatrix.trans) for all k-steps:
+  // lane L addresses row L&7 of matrix L>>3 -- matrices 0/1 = k 16s..+7,
+  // 2/3 = k 16s+8..+15; 0/2 = columns 16w..+7, 1/3 = 16w+8..+15.  BF16
+  // weights: loaded here, before the dependency wait (measured 0.01-0.03 us
+  // faster per layer call); MXFP8: after it (the dequantised tile is ready
+  // either way, and there the later load measured faster).
+  const int mi = lane >> 3;
+  const int chunk = 2 * wcol + (mi & 1);
+  uint32_t a[KS][4];
+  if constexpr (WF == kWeightBF16 && TRIG != 2) {
+    const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      return;
+    }
+  }
+  if constexpr (WF == kWeightBF16) {
+#pragma unroll
+    for (int s = 0; s < KS; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
   }
 
   // 4. Wait for the producer of q_nope / q_pe (no-op without PDL).
@@ -598,21 +639,10 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     if (c < kQChunks && m < M) qv[i] = ld_u128(p.q_nope + m * p.q_nope_ts + h * p.q_nope_hs + 8 * (c % KC));
   }
 
-  if constexpr (WF == kWeightBF16 && TRIG != 2) {
-    const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
-      return;
-    }
-  }
-  // A fragments (weights, transposed by ldmatrix.trans) for all 8 k-steps:
-  // lane L addresses row L&7 of matrix L>>3 -- matrices 0/1 = k 16s..+7,
-  // 2/3 = k 16s+8..+15; 0/2 = columns 16w..+7, 1/3 = 16w+8..+15.
-  const int mi = lane >> 3;
-  const int chunk = 2 * wcol + (mi & 1);
-  uint32_t a[KS][4];
+  if constexpr (WF == kWeightMXFP8) {
 #pragma unroll
-  for (int s = 0; s < KS; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
+    for (int s = 0; s < KS; ++s) ldmatrix_x4_trans(a[s], s_a + sw128(16 * s + 8 * (mi >> 1) + (lane & 7), chunk));
+  }
 
 #pragma unroll
   for (int i = 0; i < QI; ++i) {
@@ -625,8 +655,10 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   if (has_pe) {
     const size_t off = static_cast<size_t>(m_pe) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + kLatent +
                        2 * (j_pe & 31);
-    if (OD == kOutBF16 || table_ok) {
-      write_pe_pair<OD, kTableMode>(p, off, pe, divtab, qs, rcp);
+    if (OD == kOutBF16 || mul_ok) {
+      write_pe_pair<OD, kE4m3MulExact>(p, off, pe, divtab, qs, rcp);
+    } else if (table_ok) {
+      write_pe_pair<OD, kE4m3Table>(p, off, pe, divtab, qs, rcp);
     } else {
       write_pe_pair<OD, kE4m3Divide>(p, off, pe, divtab, qs, rcp);
     }
@@ -664,9 +696,11 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   // 7. Epilogue; the E4M3 division form is chosen once per CTA so that the
   //    common path holds no call and no branch.
   if constexpr (OD == kOutBF16) {
-    write_projection<OD, MTW, TS, kTableMode>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
+    write_projection<OD, MTW, TS, kE4m3MulExact>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
+  } else if (mul_ok) {
+    write_projection<OD, MTW, TS, kE4m3MulExact>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
   } else if (table_ok) {
-    write_projection<OD, MTW, TS, kTableMode>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
+    write_projection<OD, MTW, TS, kE4m3Table>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
   } else {
     write_projection<OD, MTW, TS, kE4m3Divide>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
   }

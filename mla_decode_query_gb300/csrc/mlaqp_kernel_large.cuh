@@ -216,14 +216,19 @@ __global__ void __launch_bounds__(large_threads(TT)) mlaqp_fused_query_large_ker
     prefetch_l2(q_pe + (tid - (kLargeThreads - 128)) * p.q_pe_ts);
   }
   uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L.div);
-  bool table_ok = false;
+  bool table_ok = false, mul_ok = false;
   float rcp = 1.f;
+  bool mine = true;
   if constexpr (OD == kOutE4M3) {
-    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the CTA
-    if (table_ok && tid < 128) divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;  // uniform across the grid
     rcp = __frcp_rn(qs);
+    mine = table_ok;
+    if (table_ok && tid < 128) {
+      divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+      mine = e4m3_mul_exact_for(tid, qs, rcp);
+    }
   }
-  __syncthreads();  // barriers initialised, table visible
+  mul_ok = __syncthreads_and(mine) && OD == kOutE4M3;  // barriers initialised, table visible
 
   // 3. MXFP8: dequantise both 64-column halves into the swizzled BF16 tile
   //    (value = code * 2^(x-127) as two exact power-of-two factors).  Job
@@ -330,8 +335,10 @@ __global__ void __launch_bounds__(large_threads(TT)) mlaqp_fused_query_large_ker
     if (j < rows * (kRope / 2)) {
       const size_t off = static_cast<size_t>(m0 + (j >> 5)) * p.out_row_stride + static_cast<size_t>(h) * kOutDim +
                          kLatent + 2 * (j & 31);
-      if (OD == kOutBF16 || table_ok) {
-        write_pe_pair<OD, kE4m3Mul>(p, off, pe[i], divtab, qs, rcp);
+      if (OD == kOutBF16 || mul_ok) {
+        write_pe_pair<OD, kE4m3MulExact>(p, off, pe[i], divtab, qs, rcp);
+      } else if (table_ok) {
+        write_pe_pair<OD, kE4m3Table>(p, off, pe[i], divtab, qs, rcp);
       } else {
         write_pe_pair<OD, kE4m3Divide>(p, off, pe[i], divtab, qs, rcp);
       }
@@ -363,9 +370,12 @@ __global__ void __launch_bounds__(large_threads(TT)) mlaqp_fused_query_large_ker
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = pack_bf16x2(__uint_as_float(r[2 * i + 1]), __uint_as_float(r[2 * i]));
     if constexpr (OD == kOutE4M3) {
-      if (table_ok) {
+      if (mul_ok) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<kE4m3Mul>(v[i], divtab, qs, rcp);
+        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<kE4m3MulExact>(v[i], divtab, qs, rcp);
+      } else if (table_ok) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<kE4m3Table>(v[i], divtab, qs, rcp);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = e4m3_pair<kE4m3Divide>(v[i], divtab, qs, rcp);

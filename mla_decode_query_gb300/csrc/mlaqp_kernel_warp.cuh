@@ -66,7 +66,7 @@ struct WarpRunParams {
   float inv_heads;              // RN(1 / H)
 };
 
-// Dynamic shared memory of one CTA (offsets from a 128-byte aligned base).
+// Dynamic shared memory of one CTA (offsets from a 1024-byte aligned base).
 template <int K>
 struct WSmem {
   static constexpr int kTileA = K * kWTileCols * 2;        // BF16 [K][16], 32-byte rows, 32B swizzle
@@ -78,47 +78,6 @@ struct WSmem {
   static constexpr int Bar = Div + 128 * 4;                      // the weight barrier
   static constexpr int Bytes = Bar + 8 + 1024;                   // + slack for the alignment
 };
-
-// True when one multiply by rcp = RN(1/q_scale) gives, for every BF16 value
-// p, the E4M3 code of the IEEE quotient RN(p / q_scale); one thread checks
-// one significand 128 + f, and the CTA takes the AND over f = 0..127.
-//
-// Why it suffices.  A normal BF16 value is p = (128 + f) * 2^j.  While the
-// results stay normal binary32 values, RN(p * rcp) = RN((128+f) * rcp) * 2^j
-// = m * 2^j and RN(p / q) = t * 2^j with t = RN((128+f) / q), because
-// rounding commutes with scaling by a power of two.  The E4M3 code of x * 2^j
-// depends on j only through the regime x * 2^j falls in: at or above 2^-6
-// (E4M3 normals and saturation) the code is the same 3-bit rounding of the
-// significand for every j, in [2^-10, 2^-6) the rounding step is 2^-9, and
-// below 2^-10 everything rounds to zero.  m and t are at most a few binary32
-// ulps apart, so comparing the codes of m * 2^k and t * 2^k with k chosen to
-// put t into each binade 2^-11 .. 2^-7 and into [1, 2) covers every j.
-// Values outside the normal range decide the same code either way (zero,
-// BF16 subnormals, infinities: +-0 or +-448) given 2^-100 <= q <= 2^100,
-// which the caller checks.  A refusal only costs speed: the CTA then uses
-// the division table.
-__device__ __forceinline__ bool e4m3_mul_exact_for(int f, float qs, float rcp) {
-  const float num = static_cast<float>(128 + f);
-  const float t = __fdiv_rn(num, qs);
-  const float m = __fmul_rn(num, rcp);
-  const int et = static_cast<int>((__float_as_uint(t) >> 23) & 0xFFu) - 127;
-  bool ok = true;
-#pragma unroll
-  for (int i = 0; i < 6; ++i) {
-    const int target = i < 5 ? -11 + i : 0;
-    const float s = __uint_as_float(static_cast<uint32_t>(target - et + 127) << 23);  // 2^(target - et)
-    const uint32_t codes = pack_e4m3x2(__fmul_rn(t, s), __fmul_rn(m, s));
-    ok = ok && ((codes & 0xFFu) == (codes >> 8));
-  }
-  return ok;
-}
-
-// E4M3 conversion forms of the warp-tile kernel, chosen once per CTA:
-//   kE4m3Divide: q_scale outside [2^-100, 2^100], IEEE division;
-//   kE4m3Table:  the division table (div_by_table);
-//   kE4m3MulExact: one multiply by RN(1/q_scale), when e4m3_mul_exact_for
-//                  held for every significand.
-constexpr int kE4m3MulExact = 3;
 
 // floor(a / d) for small non-negative integers without an integer division:
 // `inv` = 1/d (within a few float ulps; the caller passes the host's RN(1/d)
@@ -137,17 +96,6 @@ __device__ __forceinline__ int floor_div(int a, float inv) {
 // bytes (the swizzle repeats every 256).
 __device__ __forceinline__ uint32_t sw32(int k, int chunk) {
   return static_cast<uint32_t>(32 * k + 16 * (chunk ^ ((k >> 2) & 1)));
-}
-
-template <int MODE>
-__device__ __forceinline__ uint32_t e4m3_pair_w(uint32_t two_bf16, const uint32_t* tab, float qs, float rcp) {
-  if constexpr (MODE == kE4m3MulExact) {
-    return pack_e4m3x2(__fmul_rn(bf16_hi(two_bf16), rcp), __fmul_rn(bf16_lo(two_bf16), rcp));
-  } else if constexpr (MODE == kE4m3Table) {
-    return pack_e4m3x2(div_by_table(two_bf16 >> 16, tab), div_by_table(two_bf16 & 0xFFFFu, tab));
-  } else {
-    return e4m3_pair_divide(two_bf16, qs);
-  }
 }
 
 // Epilogue of the tensor-core arm for one warp: D rows g / g+8 of MMA tile i
@@ -171,8 +119,8 @@ __device__ __forceinline__ void write_tile(const WarpRunParams& p, const float (
   if constexpr (OD == kOutE4M3) {
 #pragma unroll
     for (int i = 0; i < MTW; ++i) {
-      const uint32_t lo = e4m3_pair_w<MODE>(r[i][0], divtab, qs, rcp) & 0xFFFFu;
-      const uint32_t hi = e4m3_pair_w<MODE>(r[i][1], divtab, qs, rcp) & 0xFFFFu;
+      const uint32_t lo = e4m3_pair<MODE>(r[i][0], divtab, qs, rcp) & 0xFFFFu;
+      const uint32_t hi = e4m3_pair<MODE>(r[i][1], divtab, qs, rcp) & 0xFFFFu;
       const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, (t & 1) ? lo : hi, 1);
       w4[i] = (t & 1) ? (got | (hi << 16)) : (lo | (got << 16));
     }
@@ -207,7 +155,7 @@ __device__ __forceinline__ void write_fma_token(const WarpRunParams& p, float v,
       *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + off) = pair;
     }
   } else {
-    const uint32_t codes = e4m3_pair_w<MODE>(pair, divtab, qs, rcp) & 0xFFFFu;  // columns c, c+1
+    const uint32_t codes = e4m3_pair<MODE>(pair, divtab, qs, rcp) & 0xFFFFu;  // columns c, c+1
     const uint32_t next = __shfl_down_sync(0xFFFFFFFFu, codes, 4);             // columns c+2, c+3
     if ((lane & 7) == 0 && m < p.M) {
       const size_t off = static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + n0 + (lane >> 1);
@@ -429,11 +377,11 @@ __global__ void __launch_bounds__(32 * TS * kWMaxTilesPerCta, 2) mlaqp_query_war
       if constexpr (OD == kOutBF16) {
         *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + off) = pe;
       } else if (mul_ok) {
-        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair_w<kE4m3MulExact>(pe, divtab, qs, rcp));
+        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<kE4m3MulExact>(pe, divtab, qs, rcp));
       } else if (table_ok) {
-        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair_w<kE4m3Table>(pe, divtab, qs, rcp));
+        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<kE4m3Table>(pe, divtab, qs, rcp));
       } else {
-        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair_w<kE4m3Divide>(pe, divtab, qs, rcp));
+        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<kE4m3Divide>(pe, divtab, qs, rcp));
       }
     }
     if (!active) return;
@@ -497,11 +445,11 @@ __global__ void __launch_bounds__(32 * TS * kWMaxTilesPerCta, 2) mlaqp_query_war
       if constexpr (OD == kOutBF16) {
         *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + off) = pe;
       } else if (mul_ok) {
-        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair_w<kE4m3MulExact>(pe, divtab, qs, rcp));
+        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<kE4m3MulExact>(pe, divtab, qs, rcp));
       } else if (table_ok) {
-        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair_w<kE4m3Table>(pe, divtab, qs, rcp));
+        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<kE4m3Table>(pe, divtab, qs, rcp));
       } else {
-        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair_w<kE4m3Divide>(pe, divtab, qs, rcp));
+        *reinterpret_cast<uint16_t*>(p.out + off) = static_cast<uint16_t>(e4m3_pair<kE4m3Divide>(pe, divtab, qs, rcp));
       }
     }
     if (!active) return;
