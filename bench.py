@@ -26,10 +26,13 @@ from __future__ import annotations
 
 import os
 
-# The CPU oracle legs report one core: keep numpy's BLAS single-threaded (set
-# before numpy loads it).
-os.environ["OPENBLAS_NUM_THREADS"] = "1"
-os.environ["MKL_NUM_THREADS"] = "1"
+# The CPU oracle leg runs on the host cores this process may use: numpy's
+# BLAS gets that many threads (set before numpy loads it).  A one-core figure
+# is taken in a child process with MLAQP_BENCH_BLAS_THREADS=1.
+HOST_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+BLAS_THREADS = int(os.environ.get("MLAQP_BENCH_BLAS_THREADS", str(HOST_CORES)))
+for _var in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "OMP_NUM_THREADS"):
+    os.environ[_var] = str(BLAS_THREADS)
 
 import argparse
 import json
@@ -80,7 +83,7 @@ class LayerSet:
     and output buffers laid out [L, M, H, *] so each launch reads its own."""
 
     def __init__(self, weight_format, out_dtype, n_layers, h=H, m_points=M_POINTS, device="cuda",
-                 config_index=None, nope=128, arm="auto"):
+                 config_index=None, nope=128, arm="auto", distinct=None, share=None):
         import torch
         from mla_decode_query_gb300 import inputs
 
@@ -89,27 +92,43 @@ class LayerSet:
         self.m_points = tuple(m_points)
         ci = CONFIG_INDEX[weight_format] if config_index is None else config_index
         m_max = max(32, max(self.m_points))  # the first 32 token rows do not depend on m_max
-        self.host = [inputs.make_layer(inputs.layer_seed(ci, l), h, weight_format, m_max=m_max, nope=nope)
-                     for l in range(n_layers)]
-        wdt = torch.int16 if weight_format == "bf16" else torch.uint8
-        w = np.stack([d["weight"] for d in self.host])
-        self.weight = torch.from_numpy(w.view(np.int16) if weight_format == "bf16" else w).to(device)
-        assert self.weight.dtype == wdt
-        self.scale = None
-        if weight_format == "mxfp8":
-            self.scale = torch.from_numpy(np.stack([d["weight_scale"] for d in self.host])).to(device)
+        # `distinct` < n_layers: generate that many layers and repeat them at
+        # distinct addresses (timing runs: the rotated bytes still stream from
+        # DRAM); `share`: reuse another set's weights and inputs (same format
+        # and head count, another output dtype).
+        if share is not None:
+            self.host, self.weight, self.scale = share.host, share.weight, share.scale
+        else:
+            nd = n_layers if not distinct else min(distinct, n_layers)
+            gen = [inputs.make_layer(inputs.layer_seed(ci, l), h, weight_format, m_max=m_max, nope=nope)
+                   for l in range(nd)]
+            self.host = [gen[l % nd] for l in range(n_layers)]
+            wdt = torch.int16 if weight_format == "bf16" else torch.uint8
+            w = np.stack([d["weight"] for d in gen])
+            w = torch.from_numpy(w.view(np.int16) if weight_format == "bf16" else w).to(device)
+            reps = -(-n_layers // nd)
+            self.weight = w.repeat((reps,) + (1,) * (w.dim() - 1))[:n_layers].contiguous()
+            assert self.weight.dtype == wdt
+            self.scale = None
+            if weight_format == "mxfp8":
+                sc = torch.from_numpy(np.stack([d["weight_scale"] for d in gen])).to(device)
+                self.scale = sc.repeat((reps,) + (1,) * (sc.dim() - 1))[:n_layers].contiguous()
         self.q_scale_value = np.float32(inputs.make_q_scale(Q_SCALE_SEED)) if out_dtype == "e4m3" else None
         self.q_scale = (torch.tensor([self.q_scale_value], dtype=torch.float32, device=device)
                         if out_dtype == "e4m3" else None)
         odt = torch.int16 if out_dtype == "bf16" else torch.uint8
         self.q_nope_host, self.q_pe_host, self.q_nope, self.q_pe, self.out = {}, {}, {}, {}, {}
         for M in self.m_points:
-            qn = np.stack([d["q_nope"][:M] for d in self.host]).view(np.int16)
-            qp = np.stack([d["q_pe"][:M] for d in self.host]).view(np.int16)
-            self.q_nope_host[M] = torch.from_numpy(qn).pin_memory()
-            self.q_pe_host[M] = torch.from_numpy(qp).pin_memory()
-            self.q_nope[M] = self.q_nope_host[M].to(device)
-            self.q_pe[M] = self.q_pe_host[M].to(device)
+            if share is not None:
+                self.q_nope_host[M], self.q_pe_host[M] = share.q_nope_host[M], share.q_pe_host[M]
+                self.q_nope[M], self.q_pe[M] = share.q_nope[M], share.q_pe[M]
+            else:
+                qn = np.stack([d["q_nope"][:M] for d in self.host]).view(np.int16)
+                qp = np.stack([d["q_pe"][:M] for d in self.host]).view(np.int16)
+                self.q_nope_host[M] = torch.from_numpy(qn).pin_memory()
+                self.q_pe_host[M] = torch.from_numpy(qp).pin_memory()
+                self.q_nope[M] = self.q_nope_host[M].to(device)
+                self.q_pe[M] = self.q_pe_host[M].to(device)
             self.out[M] = torch.zeros((n_layers, M, h, 576), dtype=odt, device=device)
 
     def host_inputs(self, M):
@@ -347,7 +366,18 @@ def time_oracle(budget_s, samples, m_points=M_POINTS, op="query"):
 
 
 def oracle_threads():
-    return 1
+    return BLAS_THREADS
+
+
+def oracle_one_core(budget_s, op):
+    """The same oracle timing in a child process whose BLAS has one thread."""
+    env = dict(os.environ, MLAQP_BENCH_BLAS_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-only", "--cpu-budget", str(budget_s), "--op", op]
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 4 + 120)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"error": str(e)[:200]}
 
 
 # --------------------------------------------------------------------------- main arms
@@ -435,7 +465,7 @@ def run_gpu(args):
     points = [(s, M) for s in sets for M in m_points]
     graphs = [s.capture(M, pdl=not args.no_pdl) for s, M in points]
     alt = None
-    if args.compare_no_pdl and not args.no_pdl:
+    if not args.no_pdl and not args.pdl_only:
         alt = [s.capture(M, pdl=False) for s, M in points]
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -540,17 +570,148 @@ def run_gpu(args):
             "clocks": clk,
             "e2e": e2e,
         }
+        if not args.no_extras and not v_up:
+            line["config0_isolated_call"] = isolated_calls(max(20, args.steps))
+            line["behind_producer"] = behind_producer(max(5, args.steps), args.warmup)
+            st = args.sweep_steps
+            line["config4_sweep"] = {
+                "columns": ["pair", "H", "M", "us_per_layer", "gbs"],
+                "rows": sweep([("bf16", "bf16"), ("bf16", "e4m3"), ("mxfp8", "bf16"), ("mxfp8", "e4m3")],
+                              (8, 11, 16), M_POINTS, st, args.warmup, 4)}
+            all_m = tuple(range(1, 33))
+            line["config2_points"] = {"columns": ["pair", "H", "M", "us_per_layer", "gbs"],
+                                      "rows": sweep([("mxfp8", "bf16")], (8,), all_m, st, args.warmup, 2)}
+            line["config3_points"] = {"columns": ["pair", "H", "M", "us_per_layer", "gbs"],
+                                      "rows": sweep([("mxfp8", "e4m3")], (16,), all_m, st, args.warmup, 3)}
         if not args.no_cpu_baseline:
             gbs, calls, el = time_oracle(args.cpu_budget, oracle_samples(args.op), op=args.op)
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle_threads(),
-                                    "kind": "oracle",
+                                    "host_cores": HOST_CORES, "kind": "oracle",
                                     "sample": f"{calls} oracle layer calls over 2 formats x M in "
                                               f"{{{','.join(map(str, M_POINTS))}}} (H={H}), {el:.1f} s, "
-                                              f"layer 0 of each format"}
+                                              f"layer 0 of each format; BLAS threads = usable host cores",
+                                    "one_core": oracle_one_core(max(3.0, args.cpu_budget / 2), args.op)}
         print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def time_graph(g, layers, steps, warmup, stream=None):
+    """Median over `steps` individually timed replays of graph `g`, in us per
+    layer (the graph holds `layers` layer calls)."""
+    import torch
+    stream = stream or torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return 1e3 * statistics.median(a.elapsed_time(b) for a, b in ev) / layers
+
+
+def sweep(pairs, heads, m_points, steps, warmup, config_index, distinct=32):
+    """us per layer call and GB/s of every (pair, H, M): 128-512-layer PDL
+    graph replays (at least twice the L2 of rotated weights), `distinct`
+    generated layers repeated at distinct addresses."""
+    import torch
+    rows = []
+    for h in heads:
+        base = {}
+        for fmt, od in pairs:
+            ls = LayerSet(fmt, od, layers_for(fmt, h), h=h, m_points=m_points, config_index=config_index,
+                          distinct=distinct, share=base.get(fmt))
+            base.setdefault(fmt, ls)
+            for M in m_points:
+                g = ls.capture(M)
+                us = time_graph(g, ls.L, steps, warmup)
+                rows.append([f"{fmt}->{od}", h, M, round(us, 4), round(ls.bytes_per_call(M) / (us * 1e-6) / 1e9, 1)])
+                del g
+            del ls
+        del base
+        torch.cuda.empty_cache()
+    return rows
+
+
+def isolated_calls(steps):
+    """One layer call on its own (no dependent chain): a CUDA graph of one
+    plain launch, each replay timed alone.  warm: back to back (weights in
+    L2 after the first); cold: a 256 MiB write before every replay evicts
+    the weights and inputs from L2."""
+    import torch
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for fmt, od, ci in (("bf16", "bf16", 0), ("mxfp8", "e4m3", 3)):
+        ls = LayerSet(fmt, od, 1, h=H, m_points=(1,), config_index=ci)
+        g = ls.capture(1, pdl=False)
+        warm = time_graph(g, 1, steps, 3)
+        ms = []
+        for _ in range(steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        out[f"{fmt}->{od} H{H} M1"] = {"warm_us": round(warm, 4), "cold_us": round(1e3 * statistics.median(ms), 4)}
+        del g, ls
+    return out
+
+
+def behind_producer(steps, warmup, m_points=(1, 8, 32)):
+    """The op the way a decode step runs it: each layer call follows the
+    kernels that produce its q_nope and q_pe (here two elementwise PyTorch
+    kernels writing them, which, like most producers, do not trigger
+    dependent launches early).  Graphs of 128 (BF16) / 256 (MXFP8) such
+    layer steps, with the op launched with and without PDL, against the
+    same graph of producers alone: op_us = layer step - producers."""
+    import torch
+    import mla_decode_query_gb300 as mq
+    res = []
+    for fmt, od in FORMATS:
+        ls = LayerSet(fmt, od, DEFAULT_LAYERS[fmt], h=H, m_points=m_points, distinct=32)
+        for M in m_points:
+            src_n, src_p = ls.q_nope[M].clone(), ls.q_pe[M].clone()
+
+            def producers(l):
+                torch.mul(src_n[l], 1, out=ls.q_nope[M][l])
+                torch.mul(src_p[l], 1, out=ls.q_pe[M][l])
+
+            def build(with_op, pdl):
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    for l in range(ls.L):
+                        producers(l)
+                        if with_op:
+                            run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
+                            mq.check(run(**ls.layer_args(M, l), stream=s))
+                torch.cuda.current_stream().wait_stream(s)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for l in range(ls.L):
+                        producers(l)
+                        if with_op:
+                            run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
+                            mq.check(run(**ls.layer_args(M, l)))
+                return g
+
+            gp, gpdl, gplain = build(False, False), build(True, True), build(True, False)
+            prod = time_graph(gp, ls.L, steps, warmup)
+            step_pdl = time_graph(gpdl, ls.L, steps, warmup)
+            step_plain = time_graph(gplain, ls.L, steps, warmup)
+            res.append({"pair": f"{fmt}->{od}", "H": H, "M": M, "layers": ls.L, "producers_us": round(prod, 4),
+                        "step_us_pdl": round(step_pdl, 4), "op_us_pdl": round(step_pdl - prod, 4),
+                        "step_us_no_pdl": round(step_plain, 4), "op_us_no_pdl": round(step_plain - prod, 4)})
+            del gp, gpdl, gplain
+        del ls
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(sets, graphs, points, args):
@@ -711,9 +872,19 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
+    ap.add_argument("--pdl-only", action="store_true", help="skip the graphs without PDL")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the isolated-call, behind-producer and configuration sweeps")
+    ap.add_argument("--sweep-steps", type=int, default=5, help="timed replays per point of the sweeps")
+    ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.oracle_only:  # child process of the one-core oracle figure
+        gbs, calls, el = time_oracle(args.cpu_budget, oracle_samples(args.op), op=args.op)
+        print(json.dumps({"value": round(gbs, 4), "unit": "GB/s", "cores": oracle_threads(), "calls": calls,
+                          "seconds": round(el, 2)}))
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

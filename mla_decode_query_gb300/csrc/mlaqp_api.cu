@@ -372,13 +372,14 @@ enum class Arm : int { kAuto = 0, kWarpMma = 1, kWarpFma = 2, kCtaMma = 3, kTcge
 // layer's CTAs start (and stream weights) earlier, which pays while a
 // layer's post-wait work is small; above it the warp-tile kernel's one CTA
 // per SM keeps any SM from carrying two CTAs' contraction and epilogue.
-// Measured crossovers: E4M3 output M = 9 (every H, both weight formats);
-// BF16 -> BF16 M = 9 at H = 8 and 11, 17 at H = 16; MXFP8 -> BF16 M = 13 at
-// H = 8, 17 at H = 11 and 16.  Above 32 tokens: the tcgen05 kernel.
+// Measured crossovers (first M from which the warp-tile kernel is faster):
+// M = 17 at H = 11 and 16 for every format pair; at H = 8, M = 13 (MXFP8 ->
+// BF16, BF16 -> E4M3), 15 (BF16 -> BF16), 16 (MXFP8 -> E4M3).  Above 32
+// tokens: the tcgen05 kernel.
 int warp_crossover(int weight_format, int out_dtype, int H) {
-  if (out_dtype == MLAQP_OUT_E4M3) return 9;
-  if (weight_format == MLAQP_WEIGHT_BF16) return H <= 11 ? 9 : 17;
-  return H <= 8 ? 13 : 17;
+  if (H > 8) return 17;
+  if (weight_format == MLAQP_WEIGHT_BF16) return out_dtype == MLAQP_OUT_BF16 ? 15 : 13;
+  return out_dtype == MLAQP_OUT_BF16 ? 13 : 16;
 }
 
 Arm auto_arm(int weight_format, int out_dtype, int M, int H) {

@@ -122,11 +122,9 @@ def test_arms_reject_calls_they_do_not_cover(cuda_device):
 
 def _crossover(fmt, od, h):
     # the library's measured choice: warp-tile kernel from this token count on
-    if od == "e4m3":
-        return 9
-    if fmt == "bf16":
-        return 9 if h <= 11 else 17
-    return 13 if h <= 8 else 17
+    if h > 8:
+        return 17
+    return {("bf16", "bf16"): 15, ("bf16", "e4m3"): 13, ("mxfp8", "bf16"): 13, ("mxfp8", "e4m3"): 16}[(fmt, od)]
 
 
 def test_launch_shape_follows_the_policy(cuda_device):
@@ -135,7 +133,7 @@ def test_launch_shape_follows_the_policy(cuda_device):
         for h in (8, 11, 16):
             g = min(max(sms, 8 * h), 32 * h)  # warp-tile kernel: one CTA per SM, 8..32 per head
             tpc = -(-32 // (g // h))          # tiles of the head with the fewest CTAs
-            for m in (1, 8, 9, 12, 13, 16, 17, 32):
+            for m in (1, 8, 9, 12, 13, 14, 15, 16, 17, 32):
                 st, grid, threads = mq.mlaqp_launch_shape(m, h, fmt, od)
                 assert st == mq.MLAQP_OK
                 if m >= _crossover(fmt, od, h):
