@@ -667,8 +667,9 @@ def behind_producer(steps, warmup, m_points=(1, 8, 32)):
     kernels that produce its q_nope and q_pe (here two elementwise PyTorch
     kernels writing them, which, like most producers, do not trigger
     dependent launches early).  Graphs of 128 (BF16) / 256 (MXFP8) such
-    layer steps, with the op launched with and without PDL, against the
-    same graph of producers alone: op_us = layer step - producers."""
+    layer steps, with the op launched with and without PDL, and with and
+    without mlaqp_prefetch_weights on a parallel branch forked before the
+    producers; op_us = layer step - the same graph without the op."""
     import torch
     import mla_decode_query_gb300 as mq
     res = []
@@ -681,34 +682,47 @@ def behind_producer(steps, warmup, m_points=(1, 8, 32)):
                 torch.mul(src_n[l], 1, out=ls.q_nope[M][l])
                 torch.mul(src_p[l], 1, out=ls.q_pe[M][l])
 
-            def build(with_op, pdl):
+            side = torch.cuda.Stream()
+
+            def layer_step(l, with_op, pdl, prefetch):
+                main = torch.cuda.current_stream()
+                if prefetch:  # a parallel branch that warms L2 with this layer's weights
+                    side.wait_stream(main)
+                    with torch.cuda.stream(side):
+                        a = ls.layer_args(M, l)
+                        mq.check(mq.mlaqp_prefetch_weights(a["weight"], a["weight_scale"], ls.H, ls.K,
+                                                           ls.weight_format, stream=side))
+                producers(l)
+                if with_op:
+                    run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
+                    mq.check(run(**ls.layer_args(M, l), stream=main))
+                if prefetch:
+                    main.wait_stream(side)
+
+            def build(with_op, pdl, prefetch=False):
                 s = torch.cuda.Stream()
                 s.wait_stream(torch.cuda.current_stream())
                 with torch.cuda.stream(s):
                     for l in range(ls.L):
-                        producers(l)
-                        if with_op:
-                            run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
-                            mq.check(run(**ls.layer_args(M, l), stream=s))
+                        layer_step(l, with_op, pdl, prefetch)
                 torch.cuda.current_stream().wait_stream(s)
                 torch.cuda.synchronize()
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
                     for l in range(ls.L):
-                        producers(l)
-                        if with_op:
-                            run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
-                            mq.check(run(**ls.layer_args(M, l)))
+                        layer_step(l, with_op, pdl, prefetch)
                 return g
 
-            gp, gpdl, gplain = build(False, False), build(True, True), build(True, False)
-            prod = time_graph(gp, ls.L, steps, warmup)
-            step_pdl = time_graph(gpdl, ls.L, steps, warmup)
-            step_plain = time_graph(gplain, ls.L, steps, warmup)
-            res.append({"pair": f"{fmt}->{od}", "H": H, "M": M, "layers": ls.L, "producers_us": round(prod, 4),
-                        "step_us_pdl": round(step_pdl, 4), "op_us_pdl": round(step_pdl - prod, 4),
-                        "step_us_no_pdl": round(step_plain, 4), "op_us_no_pdl": round(step_plain - prod, 4)})
-            del gp, gpdl, gplain
+            row = {"pair": f"{fmt}->{od}", "H": H, "M": M, "layers": ls.L}
+            prod = time_graph(build(False, False), ls.L, steps, warmup)
+            prod_pf = time_graph(build(False, False, True), ls.L, steps, warmup)
+            row["producers_us"] = round(prod, 4)
+            for name, pdl, pf in (("pdl", True, False), ("no_pdl", False, False),
+                                  ("pdl_prefetch", True, True), ("no_pdl_prefetch", False, True)):
+                step = time_graph(build(True, pdl, pf), ls.L, steps, warmup)
+                row[f"step_us_{name}"] = round(step, 4)
+                row[f"op_us_{name}"] = round(step - (prod_pf if pf else prod), 4)
+            res.append(row)
         del ls
         torch.cuda.empty_cache()
     return res

@@ -169,6 +169,26 @@ int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q
                       int weight_format, int out_dtype, int pdl, mlaqp_stream_t stream);
 
 /*
+ * Optional L2 warm-up of one layer's weights (vLLM PR #174, section
+ * Performance evidence: the per-layer query time inside a decode step,
+ * where the kernel before this op produces q_nope / q_pe and usually does
+ * not let dependent kernels start early).  Launches one small kernel on
+ * `stream` that asks the GPU to fetch `weight` ([H, nope_dim, 512], BF16 or
+ * E4M3) and `weight_scale` ([H, nope_dim, 16] E8M0 for MXFP8, else NULL)
+ * into L2 and returns without waiting for the data; a following mlaqp_run
+ * of the same layer then finds its weights in L2.  Place it before the
+ * kernels that produce q_nope / q_pe, ideally on a parallel branch (a forked
+ * stream or graph branch), and not so early that other traffic evicts the
+ * ~1-2 MB again.  pdl != 0 launches it with programmatic dependent launch:
+ * it never waits for the previous kernel and lets the next one launch at
+ * once.  Same pointer rules as mlaqp_run; no allocation, graph-capturable.
+ * Returns MLAQP_OK, MLAQP_ERR_UNSUPPORTED, MLAQP_ERR_INVALID_ARG or
+ * MLAQP_ERR_CUDA.
+ */
+int mlaqp_prefetch_weights(const void* weight, const void* weight_scale, int num_heads, int nope_dim,
+                           int weight_format, int pdl, mlaqp_stream_t stream);
+
+/*
  * Launch geometry a run with these arguments uses (for reporting): grid size
  * in CTAs and threads per CTA.  Returns MLAQP_OK or MLAQP_ERR_UNSUPPORTED.
  */

@@ -35,6 +35,7 @@ from .mlaqp import (  # noqa: F401
     mlaqp_device_status,
     mlaqp_last_error,
     mlaqp_launch_shape,
+    mlaqp_prefetch_weights,
     mlaqp_prewarm,
     mlaqp_run,
     mlaqp_run_pdl,

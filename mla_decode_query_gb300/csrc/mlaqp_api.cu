@@ -34,6 +34,24 @@ __global__ void mlaqp_null_kernel() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// L2 warm-up of one layer's weights: CTA b asks the TMA unit of its SM to
+// fetch bytes [b*chunk, (b+1)*chunk) of the weights (then the scales) into
+// L2 and exits; nothing waits for the data.  It reads only the weights, so
+// it lets the next kernel launch at once and never waits for the previous.
+__global__ void mlaqp_prefetch_kernel(const uint8_t* w, unsigned long long w_bytes, const uint8_t* sc,
+                                      unsigned long long sc_bytes, unsigned int chunk) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x != 0) return;
+  const unsigned long long w_chunks = (w_bytes + chunk - 1) / chunk;
+  const unsigned long long b = blockIdx.x;
+  const uint8_t* base = b < w_chunks ? w : sc;
+  const unsigned long long total = b < w_chunks ? w_bytes : sc_bytes;
+  const unsigned long long off = (b < w_chunks ? b : b - w_chunks) * chunk;
+  if (off >= total) return;
+  const unsigned long long n = total - off < chunk ? total - off : chunk;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(static_cast<unsigned>(n)) : "memory");
+}
+
 using mlaqp::KernelInfo;
 using mlaqp::RunParams;
 
@@ -883,6 +901,49 @@ int mlaqp_debug_set_policy(int trig, int cta_cap) {
     return fail(MLAQP_ERR_INVALID_ARG, "trig must be -1, 0 or 1 and cta_cap in 0..8");
   g_policy_cap.store(cta_cap, std::memory_order_relaxed);
   g_policy_trig.store(trig, std::memory_order_relaxed);
+  return MLAQP_OK;
+}
+
+int mlaqp_prefetch_weights(const void* weight, const void* weight_scale, int H, int nope_dim, int weight_format,
+                           int pdl, mlaqp_stream_t stream) {
+  if (weight_format != MLAQP_WEIGHT_BF16 && weight_format != MLAQP_WEIGHT_MXFP8)
+    return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format");
+  if (!supported_heads(H)) return fail(MLAQP_ERR_UNSUPPORTED, "num_heads must be 8, 11 or 16");
+  if (nope_index(nope_dim) < 0) return fail(MLAQP_ERR_UNSUPPORTED, "nope_dim must be 128 or 192");
+  const bool mx = weight_format == MLAQP_WEIGHT_MXFP8;
+  if (!weight) return fail(MLAQP_ERR_INVALID_ARG, "weight is required");
+  if (mx && !weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "MXFP8 weights require weight_scale");
+  if (!mx && weight_scale) return fail(MLAQP_ERR_INVALID_ARG, "BF16 weights take no weight_scale (pass NULL)");
+  if (!aligned(weight, 16) || (weight_scale && !aligned(weight_scale, 16)))
+    return fail(MLAQP_ERR_INVALID_ARG, "weight and weight_scale must be 16-byte aligned");
+  int device = 0;
+  int st = resolve_device(-1, &device);
+  if (st != MLAQP_OK) return st;
+  st = check_device(device);
+  if (st != MLAQP_OK) return st;
+  const unsigned long long w_bytes =
+      static_cast<unsigned long long>(H) * nope_dim * MLAQP_LATENT_DIM * (mx ? 1 : 2);
+  const unsigned long long sc_bytes = mx ? w_bytes / 32 : 0;
+  constexpr unsigned kChunk = 64u << 10;  // per CTA (one TMA prefetch)
+  const unsigned ctas = static_cast<unsigned>((w_bytes + kChunk - 1) / kChunk + (sc_bytes + kChunk - 1) / kChunk);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const uint8_t* w = static_cast<const uint8_t*>(weight);
+  const uint8_t* sc = static_cast<const uint8_t*>(weight_scale);
+  unsigned chunk = kChunk;
+  void* args[5] = {&w, const_cast<unsigned long long*>(&w_bytes), &sc, const_cast<unsigned long long*>(&sc_bytes),
+                   &chunk};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&mlaqp_prefetch_kernel), args);
+  if (e != cudaSuccess) return fail_cuda("cudaLaunchKernelExC", e);
   return MLAQP_OK;
 }
 

@@ -62,6 +62,7 @@ _SIGNATURES = {
                                      ctypes.c_int64, _c_void_p, _c_void_p, _c_void_p, ctypes.c_int64, _c_void_p,
                                      _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
     "mlaqp_debug_set_policy": (_c_int, [_c_int, _c_int]),
+    "mlaqp_prefetch_weights": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
     "mlaqp_launch_shape": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_int),
                                     ctypes.POINTER(_c_int)]),
     "mlaqp_device_status": (_c_int, [ctypes.POINTER(ctypes.c_uint), _c_int]),
@@ -175,6 +176,12 @@ def mlaqp_run_strided(q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_p
         int(q_pe_head_stride), _ptr(weight), _ptr(weight_scale), _ptr(out), int(out_row_stride), _ptr(q_scale),
         int(M), int(H), int(nope_dim), _fmt(weight_format, WEIGHT_FORMATS), _fmt(out_dtype, OUT_DTYPES),
         1 if pdl else 0, _stream(stream))
+
+
+def mlaqp_prefetch_weights(weight, weight_scale, H, nope_dim, weight_format, pdl=False, stream=None) -> int:
+    return load_library().mlaqp_prefetch_weights(_ptr(weight), _ptr(weight_scale), int(H), int(nope_dim),
+                                                 _fmt(weight_format, WEIGHT_FORMATS), 1 if pdl else 0,
+                                                 _stream(stream))
 
 
 ARMS = {"auto": 0, "warp_mma": 1, "warp_fma": 2, "cta_mma": 3, "tcgen05": 4}

@@ -197,3 +197,19 @@ def test_v_up_zero_tokens_and_domain(built_library):
         a = dict(num_heads=16, max_m=32, weight_format="bf16")
         a.update(bad)
         assert mq.mlaqp_v_up_can_implement(**a) == 0, bad
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(weight_format=7), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(H=12), mq.MLAQP_ERR_UNSUPPORTED),
+    (dict(nope_dim=64), mq.MLAQP_ERR_UNSUPPORTED),
+    (dict(weight=None), mq.MLAQP_ERR_INVALID_ARG),
+    (dict(weight=0x1008), mq.MLAQP_ERR_INVALID_ARG),              # not 16-byte aligned
+    (dict(weight_scale=0x2000), mq.MLAQP_ERR_INVALID_ARG),        # BF16 weights take no scales
+    (dict(weight_format="mxfp8", weight_scale=None), mq.MLAQP_ERR_INVALID_ARG),
+])
+def test_prefetch_validation(built_library, kw, code):
+    # Every argument check runs before the device is touched.
+    a = dict(weight=0x1000, weight_scale=None, H=16, nope_dim=128, weight_format="bf16", stream=0)
+    a.update(kw)
+    assert mq.mlaqp_prefetch_weights(**a) == code, mq.mlaqp_last_error()

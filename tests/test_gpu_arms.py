@@ -182,3 +182,39 @@ def test_pdl_chain_alternating_arms(cuda_device, fmt, od):
         d = layers[l]
         ref, acc = oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs_val)
         check_output(_rows(outs[l], M, H, D * H, od), ref, acc, od, f"layer {l} ({arms[l % 4]})")
+
+
+@pytest.mark.parametrize("fmt,od", [("bf16", "bf16"), ("mxfp8", "e4m3")])
+def test_prefetch_weights_then_run(cuda_device, fmt, od):
+    # The L2 warm-up on a parallel graph branch, then the layer call: same
+    # results, in a graph replayed twice and eagerly.
+    H, M = 16, 5
+    d = inputs.make_layer(inputs.layer_seed(24, 0), H, fmt)
+    t = _dev(d)
+    qs_val = inputs.make_q_scale(8) if od == "e4m3" else None
+    qs = None if qs_val is None else torch.tensor([qs_val], dtype=torch.float32, device="cuda")
+    out = torch.zeros((M * D * H,), dtype=torch.int16 if od == "bf16" else torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+
+    def step():
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            for pdl in (False, True):
+                assert mq.mlaqp_prefetch_weights(t["weight"], t["weight_scale"], H, 128, fmt, pdl=pdl,
+                                                 stream=side) == mq.MLAQP_OK, mq.mlaqp_last_error()
+        assert mq.mlaqp_run_pdl(t["q_nope"], t["q_pe"], t["weight"], t["weight_scale"], out, D * H, qs, M, H,
+                                fmt, od) == mq.MLAQP_OK, mq.mlaqp_last_error()
+        main.wait_stream(side)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    ref, acc = oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs_val)
+    check_output(_rows(out, M, H, D * H, od), ref, acc, od, f"prefetch {fmt}->{od}")
