@@ -140,6 +140,10 @@ class LayerSet:
     def kernel_name(self, M):
         if self.arm == "tcgen05" or (self.arm == "auto" and M > 32):
             return "mlaqp_fused_query_large_kernel"
+        if self.arm == "auto":
+            import mla_decode_query_gb300 as mq
+            st, grid, _ = mq.mlaqp_launch_shape(M, self.H, self.weight_format, self.out_dtype)
+            return "mlaqp_fused_query_kernel" if st == 0 and grid == 8 * self.H else "mlaqp_query_warp_kernel"
         return "mlaqp_fused_query_kernel" if self.arm == "cta_mma" else "mlaqp_query_warp_kernel"
 
     def layer_args(self, M, l):
@@ -792,7 +796,10 @@ def run_e2e(sets, graphs, points, args):
 
 
 KERNEL_SOURCES = ("mla_decode_query_gb300/csrc/mlaqp_kernel.cuh", "mla_decode_query_gb300/csrc/mlaqp_kernels_bf16.cu",
-                  "mla_decode_query_gb300/csrc/mlaqp_kernels_mxfp8.cu")
+                  "mla_decode_query_gb300/csrc/mlaqp_kernels_mxfp8.cu",
+                  "mla_decode_query_gb300/csrc/mlaqp_kernel_warp.cuh",
+                  "mla_decode_query_gb300/csrc/mlaqp_kernels_warp_bf16.cu",
+                  "mla_decode_query_gb300/csrc/mlaqp_kernels_warp_mxfp8.cu")
 TRAFFIC_FILE = "profiles/fused_query_dram_traffic_h16.txt"
 
 
