@@ -89,6 +89,7 @@ class LayerSet:
 
         self.weight_format, self.out_dtype, self.L, self.H, self.K = weight_format, out_dtype, n_layers, h, nope
         self.arm = arm
+        self.pdl_mode = 1
         self.m_points = tuple(m_points)
         ci = CONFIG_INDEX[weight_format] if config_index is None else config_index
         m_max = max(32, max(self.m_points))  # the first 32 token rows do not depend on m_max
@@ -162,13 +163,13 @@ class LayerSet:
                                                 a["q_scale"], M, self.H, self.K, self.weight_format, self.out_dtype,
                                                 pdl=pdl, arm=self.arm, stream=stream))
             return
-        if self.K != 128:  # the general entry point: nope dim and (contiguous) strides
+        if self.K != 128 or (pdl and self.pdl_mode == 2):  # the general entry point: nope dim, strides, pdl mode
             for l in range(self.L):
                 a = self.layer_args(M, l)
                 mq.check(mq.mlaqp_run_strided(a["q_nope"], self.H * self.K, self.K, a["q_pe"], self.H * 64, 64,
                                               a["weight"], a["weight_scale"], a["out"], a["out_row_stride"],
                                               a["q_scale"], M, self.H, self.K, self.weight_format, self.out_dtype,
-                                              pdl=pdl, stream=stream))
+                                              pdl=self.pdl_mode if pdl else 0, stream=stream))
             return
         run = mq.mlaqp_run_pdl if pdl else mq.mlaqp_run
         for l in range(self.L):
@@ -202,6 +203,7 @@ class VLayerSet:
         from mla_decode_query_gb300 import inputs
 
         self.weight_format, self.out_dtype, self.L, self.H = weight_format, "bf16", n_layers, h
+        self.pdl_mode = 1
         self.m_points = tuple(m_points)
         ci = V_CONFIG_INDEX[weight_format]
         m_max = max(32, max(self.m_points))
@@ -232,7 +234,8 @@ class VLayerSet:
         for l in range(self.L):
             mq.check(mq.mlaqp_v_up_run(self.x[M][l], self.H * 512, 512, self.weight[l],
                                        None if self.scale is None else self.scale[l], self.out[M][l],
-                                       128 * self.H, M, self.H, self.weight_format, pdl=pdl, stream=stream))
+                                       128 * self.H, M, self.H, self.weight_format,
+                                       pdl=self.pdl_mode if pdl else 0, stream=stream))
 
     def capture(self, M, pdl=True):
         import torch
@@ -464,6 +467,9 @@ def run_gpu(args):
             sets.append(VLayerSet(fmt, L, h=h, m_points=m_points) if v_up else
                         LayerSet(fmt, od, L, h=h, m_points=m_points, nope=args.nope, arm=args.arm))
 
+    for s in sets:
+        s.pdl_mode = args.pdl_mode
+
     def key(s):
         return f"{s.weight_format}->{s.out_dtype}" + (f" H{s.H}" if multi else "")
     points = [(s, M) for s in sets for M in m_points]
@@ -562,6 +568,7 @@ def run_gpu(args):
                        "heads": heads[0] if not multi else list(heads), "nope_dim": args.nope,
                        "m_points": list(m_points), "arm": args.arm,
                        **({"policy": args.policy} if args.policy else {}),
+                       **({"pdl_mode": args.pdl_mode} if args.pdl_mode != 1 else {}),
                        "layers": {key(s): s.L for s in sets}, "pdl": not args.no_pdl,
                        "l2": f"rotated weights per replay {[s.L * s.bytes_per_call(1) >> 20 for s in sets]} MiB "
                              f"vs L2 {L2_BYTES >> 20} MiB (inputs larger than L2, no flush)",
@@ -894,6 +901,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing")
     ap.add_argument("--pdl-only", action="store_true", help="skip the graphs without PDL")
+    ap.add_argument("--pdl-mode", type=int, default=1, choices=(1, 2),
+                    help="2: opt-in early trigger of the tcgen05 kernels (tensor-memory contract of pdl = 2)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the isolated-call, behind-producer and configuration sweeps")
     ap.add_argument("--sweep-steps", type=int, default=5, help="timed replays per point of the sweeps")

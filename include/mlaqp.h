@@ -150,7 +150,7 @@ int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
                   mlaqp_stream_t stream);
 
 /*
- * General form of mlaqp_run / mlaqp_run_pdl (pdl != 0): the same operation
+ * General form of mlaqp_run (pdl = 0) / mlaqp_run_pdl (pdl = 1): the same operation
  * with nope dim `nope_dim` (128 or 192) and strided inputs, so that q_nope
  * and q_pe can be views into the upstream per-head [.., nope_dim + 64]
  * projection output, or head-major [H, M, nope_dim] (the layout of the
@@ -161,6 +161,18 @@ int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
  * (16-byte rows), q_pe strides multiples of 2.  weight is [H, nope_dim, 512]
  * (BF16 or E4M3) and weight_scale [H, nope_dim, 16]; everything else is as
  * for mlaqp_run.
+ *
+ * pdl = 2 (opt-in, no counterpart on the pages): as pdl = 1, and for
+ * M > 32 the tcgen05 kernel lets the next kernel on the stream launch at
+ * its entry rather than after it has allocated tensor memory (about 0.5 us
+ * less per layer call in a chain).  The caller promises the tensor-memory
+ * contract this needs: no kernel launched after this call on `stream`, while
+ * it may still be running, allocates tensor memory (tcgen05.alloc) before
+ * its own dependency wait -- otherwise such a kernel could hold the columns
+ * this call is waiting for while it waits for this call, and neither would
+ * finish.  Every kernel of this library allocates tensor memory only after
+ * its dependency wait, so chains of its calls meet the contract.  For
+ * M <= 32, pdl = 2 is pdl = 1.  Other values return MLAQP_ERR_INVALID_ARG.
  */
 int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride,
                       const void* q_pe, int64_t q_pe_token_stride, int64_t q_pe_head_stride,
@@ -298,9 +310,13 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *                  tensor memory is taken after the dependency wait and
  *                  freed before it returns)
  *   H              8, 11 or 16
- *   pdl            != 0: programmatic dependent launch, as mlaqp_run_pdl (the
+ *   pdl            1: programmatic dependent launch, as mlaqp_run_pdl (the
  *                  weights and scales must not be written by any kernel that
- *                  may still be running, see mlaqp_run_pdl)
+ *                  may still be running, see mlaqp_run_pdl); 2: the same,
+ *                  and above M = 64 the next kernel may launch at this one's
+ *                  entry, under the tensor-memory contract of
+ *                  mlaqp_run_strided's pdl = 2; 0: ordinary launch; other
+ *                  values return MLAQP_ERR_INVALID_ARG
  * Status codes as for mlaqp_run.
  */
 #define MLAQP_V_HEAD_DIM 128

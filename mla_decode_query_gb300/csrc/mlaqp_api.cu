@@ -253,8 +253,8 @@ const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int 
 // to M = 128, 128 above (at most 2 chunks, so one CTA per SM at H = 16).
 int large_tile_index(int M) { return M <= 64 ? 0 : M <= 128 ? 1 : 2; }
 
-const KernelInfo* lookup_large(int weight_format, int out_dtype, int nope_idx, int tile_idx) {
-  return &mlaqp::kernels_large_m()[nope_idx][tile_idx][weight_format][out_dtype];
+const KernelInfo* lookup_large(int weight_format, int out_dtype, int nope_idx, int tile_idx, int early = 0) {
+  return &mlaqp::kernels_large_m()[nope_idx][tile_idx][weight_format][out_dtype][early];
 }
 
 // Chunks of one token tile in a large-M call (grid.z).
@@ -296,15 +296,19 @@ int setup_kernels(const DeviceInfo& d) {
     for (int ti = 0; ti < 3; ++ti)
       for (int wf = 0; wf < 2; ++wf)
         for (int od = 0; od < 2; ++od) {
-          const cudaError_t e = cudaFuncSetAttribute(lookup_large(wf, od, ki, ti)->fn,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
-          if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+          for (int early = 0; early < 2; ++early) {
+            const cudaError_t e = cudaFuncSetAttribute(lookup_large(wf, od, ki, ti, early)->fn,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
+            if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+          }
         }
   for (int wf = 0; wf < 2; ++wf)
     for (int ti = 0; ti < 2; ++ti) {
-      const cudaError_t e = cudaFuncSetAttribute(mlaqp::kernels_v_up_large()[wf][ti].fn,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
-      if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+      for (int early = 0; early < 2; ++early) {
+        const cudaError_t e = cudaFuncSetAttribute(mlaqp::kernels_v_up_large()[wf][ti][early].fn,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin);
+        if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+      }
     }
   for (int wf = 0; wf < 2; ++wf) {
     const mlaqp::WarpKernelSet& set = wf == 0 ? mlaqp::kernels_warp_bf16_weights() : mlaqp::kernels_warp_mxfp8_weights();
@@ -390,19 +394,24 @@ enum class Arm : int { kAuto = 0, kWarpMma = 1, kWarpFma = 2, kCtaMma = 3, kTcge
 // layer's CTAs start (and stream weights) earlier, which pays while a
 // layer's post-wait work is small; above it the warp-tile kernel's one CTA
 // per SM keeps any SM from carrying two CTAs' contraction and epilogue.
-// Measured crossovers (first M from which the warp-tile kernel is faster):
-// M = 17 at H = 11 and 16 for every format pair; at H = 8, M = 13 (MXFP8 ->
-// BF16, BF16 -> E4M3), 15 (BF16 -> BF16), 16 (MXFP8 -> E4M3).  Above 32
-// tokens: the tcgen05 kernel.
+// Measured crossovers (first M from which the warp-tile kernel is faster),
+// nope dim 128: M = 17 at H = 11 and 16 for every format pair; at H = 8,
+// M = 13 (MXFP8 -> BF16, BF16 -> E4M3), 15 (BF16 -> BF16), 16 (MXFP8 ->
+// E4M3).  Nope dim 192 (H = 16): the warp-tile kernel from M = 17, but for
+// M = 25..32 (four token tiles, 12 k-steps) only with BF16 weights and E4M3
+// output.  Above 32 tokens: the tcgen05 kernel.
 int warp_crossover(int weight_format, int out_dtype, int H) {
   if (H > 8) return 17;
   if (weight_format == MLAQP_WEIGHT_BF16) return out_dtype == MLAQP_OUT_BF16 ? 15 : 13;
   return out_dtype == MLAQP_OUT_BF16 ? 13 : 16;
 }
 
-Arm auto_arm(int weight_format, int out_dtype, int M, int H) {
+Arm auto_arm(int weight_format, int out_dtype, int M, int H, int K) {
   if (M > MLAQP_MAX_M_DECODE) return Arm::kTcgen05;
-  return M >= warp_crossover(weight_format, out_dtype, H) ? Arm::kWarpMma : Arm::kCtaMma;
+  if (M < warp_crossover(weight_format, out_dtype, H)) return Arm::kCtaMma;
+  if (K != MLAQP_NOPE_DIM && M > 24 && !(weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3))
+    return Arm::kCtaMma;
+  return Arm::kWarpMma;
 }
 
 // Grid of a warp-tile launch: one CTA per SM, but at least 8 CTAs per head
@@ -437,7 +446,7 @@ LaunchPolicy warp_launch_policy(int /*weight_format*/, int /*out_dtype*/, int /*
   return LaunchPolicy{0, 2};
 }
 
-int launch_warp(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx,
+int launch_warp(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long long wait_limit_ns, unsigned extra_tx,
                 Arm arm, int device) {
   const int M = a.M, H = a.H, K = a.K;
   const bool mx = a.weight_format == MLAQP_WEIGHT_MXFP8;
@@ -483,8 +492,12 @@ int launch_warp(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long
   return MLAQP_OK;
 }
 
-int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx,
+// pdl: 0 = ordinary launch, 1 = programmatic dependent launch, 2 = the same
+// with the tcgen05 kernel's next-kernel trigger at entry (the caller's
+// opt-in under the tensor-memory contract stated in the header).
+int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long long wait_limit_ns, unsigned extra_tx,
              Arm forced = Arm::kAuto) {
+  if (pdl < 0 || pdl > 2) return fail(MLAQP_ERR_INVALID_ARG, "pdl must be 0, 1 or 2");
   const int M = a.M, H = a.H, K = a.K;
   if (!valid_enums(a.weight_format, a.out_dtype)) return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format or out_dtype");
   if (M < 0) return fail(MLAQP_ERR_INVALID_ARG, "M must be >= 0");
@@ -540,7 +553,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   if (st != MLAQP_OK) return st;
 
   Arm arm = forced;
-  if (arm == Arm::kAuto) arm = auto_arm(a.weight_format, a.out_dtype, M, H);
+  if (arm == Arm::kAuto) arm = auto_arm(a.weight_format, a.out_dtype, M, H, K);
   if (arm == Arm::kWarpFma && (M > 8 || K != 128))
     return fail(MLAQP_ERR_UNSUPPORTED, "the CUDA-core arm covers M <= 8 at nope_dim 128");
   if ((arm == Arm::kWarpMma || arm == Arm::kCtaMma) && M > MLAQP_MAX_M_DECODE)
@@ -551,7 +564,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
   const KernelInfo* k = nullptr;
   int smem_bytes = 0;
   if (large) {
-    k = lookup_large(a.weight_format, a.out_dtype, ki, large_tile_index(M));
+    k = lookup_large(a.weight_format, a.out_dtype, ki, large_tile_index(M), pdl == 2 ? 1 : 0);
     smem_bytes = large_smem(g_dev[device], k->smem_bytes, M);
   } else {
     const LaunchPolicy pol = launch_policy(a.weight_format, a.out_dtype, M);
@@ -600,9 +613,10 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long lo
 // ---------------------------------------------------------------------------
 
 // 2-D tensor map over W_UV viewed as [H*512 rows][128 columns].  For the
-// M <= 32 kernel one box is 16 columns x 256 rows, unswizzled (a CTA copies
-// two); for the cluster kernel 64 columns x 128 rows, 128B-swizzled for BF16
-// (the UMMA operand layout) and unswizzled for E4M3 (a CTA copies two).
+// M <= 64 kernel one box is 16 columns x 256 rows (a CTA copies two), BF16
+// with the 32-byte swizzle (conflict-free ldmatrix of its 32-byte rows),
+// E4M3 unswizzled; for the cluster kernel 64 columns x 128 rows,
+// 128B-swizzled for BF16 (the UMMA operand layout) and unswizzled for E4M3.
 int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx, bool large) {
   std::string err;
   EncodeTiledFn fn = encode_tiled_fn(&err);
@@ -615,7 +629,7 @@ int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx, bo
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                         const_cast<void*>(weight), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        large && !mx ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        mx ? CU_TENSOR_MAP_SWIZZLE_NONE : (large ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B),
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MLAQP_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
   return MLAQP_OK;
@@ -641,8 +655,8 @@ const KernelInfo* lookup_v_up(int weight_format, int M, int trig) {
 // MXFP8, against 5.07 / 5.75).
 int v_large_tile_index(int M) { return M <= 128 ? 0 : 1; }
 
-const KernelInfo* lookup_v_up_large(int weight_format, int M) {
-  return &mlaqp::kernels_v_up_large()[weight_format][v_large_tile_index(M)];
+const KernelInfo* lookup_v_up_large(int weight_format, int M, int early) {
+  return &mlaqp::kernels_v_up_large()[weight_format][v_large_tile_index(M)][early];
 }
 
 struct VUpArgs {
@@ -655,7 +669,8 @@ struct VUpArgs {
   int M, H, weight_format;
 };
 
-int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
+int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
+  if (pdl < 0 || pdl > 2) return fail(MLAQP_ERR_INVALID_ARG, "pdl must be 0, 1 or 2");
   const int M = a.M, H = a.H;
   if (a.weight_format != MLAQP_WEIGHT_BF16 && a.weight_format != MLAQP_WEIGHT_MXFP8)
     return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format");
@@ -697,7 +712,7 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, bool pdl, unsigned long l
   int smem_bytes = 0;
   int chunks = 0;
   if (large) {
-    k = lookup_v_up_large(a.weight_format, M);
+    k = lookup_v_up_large(a.weight_format, M, pdl == 2 ? 1 : 0);
     const int tt = mlaqp::kVLargeTokTiles[v_large_tile_index(M)];
     chunks = (M + tt - 1) / tt;
     smem_bytes = tmem_safe_smem(g_dev[device], k->smem_bytes, ((M < tt ? M : tt) + 15) & ~15);
@@ -812,7 +827,8 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
     for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)
       for (int ti = 0; ti < 3 && status == MLAQP_OK; ++ti) {
         cudaFuncAttributes attr;
-        e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti)->fn);
+        e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti, 0)->fn);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti, 1)->fn);
         if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
       }
     if (status == MLAQP_OK) g_prewarmed[dev].fetch_or(large_bit, std::memory_order_acq_rel);
@@ -826,7 +842,7 @@ int mlaqp_run(const void* q_nope, const void* q_pe, const void* weight, const vo
               mlaqp_stream_t stream) {
   return run_impl(contiguous_args(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H,
                                   weight_format, out_dtype),
-                  stream, false, kDefaultWaitLimitNs, 0);
+                  stream, 0, kDefaultWaitLimitNs, 0);
 }
 
 int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight, const void* weight_scale, void* out,
@@ -834,7 +850,7 @@ int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight, cons
                   mlaqp_stream_t stream) {
   return run_impl(contiguous_args(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H,
                                   weight_format, out_dtype),
-                  stream, true, kDefaultWaitLimitNs, 0);
+                  stream, 1, kDefaultWaitLimitNs, 0);
 }
 
 int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride, const void* q_pe,
@@ -843,7 +859,7 @@ int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q
                       int H, int nope_dim, int weight_format, int out_dtype, int pdl, mlaqp_stream_t stream) {
   const RunArgs a{q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_pe_token_stride, q_pe_head_stride,
                   weight, weight_scale, out, out_row_stride, q_scale, M, H, nope_dim, weight_format, out_dtype};
-  return run_impl(a, stream, pdl != 0, kDefaultWaitLimitNs, 0);
+  return run_impl(a, stream, pdl, kDefaultWaitLimitNs, 0);
 }
 
 int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas, int* threads_per_cta) {
@@ -855,7 +871,7 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
     if (threads_per_cta) *threads_per_cta = k->threads;
     return MLAQP_OK;
   }
-  if (auto_arm(weight_format, out_dtype, M, H) == Arm::kCtaMma) {
+  if (auto_arm(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM) == Arm::kCtaMma) {
     const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0);
     if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
     if (threads_per_cta) *threads_per_cta = k->threads;
@@ -882,7 +898,7 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
   if (extra_tx_bytes > (1u << 19)) return fail(MLAQP_ERR_INVALID_ARG, "extra_tx_bytes must be <= 2^19");
   return run_impl(contiguous_args(q_nope, q_pe, weight, weight_scale, out, out_row_stride, q_scale, M, H,
                                   weight_format, out_dtype),
-                  stream, false, wait_limit_ns, extra_tx_bytes);
+                  stream, 0, wait_limit_ns, extra_tx_bytes);
 }
 
 int mlaqp_debug_run_arm(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride, const void* q_pe,
@@ -893,7 +909,7 @@ int mlaqp_debug_run_arm(const void* q_nope, int64_t q_nope_token_stride, int64_t
   if (arm < 0 || arm > 4) return fail(MLAQP_ERR_INVALID_ARG, "arm must be in 0..4");
   const RunArgs a{q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_pe_token_stride, q_pe_head_stride,
                   weight, weight_scale, out, out_row_stride, q_scale, M, H, nope_dim, weight_format, out_dtype};
-  return run_impl(a, stream, pdl != 0, kDefaultWaitLimitNs, 0, static_cast<Arm>(arm));
+  return run_impl(a, stream, pdl, kDefaultWaitLimitNs, 0, static_cast<Arm>(arm));
 }
 
 int mlaqp_debug_set_policy(int trig, int cta_cap) {
@@ -985,7 +1001,7 @@ int mlaqp_v_up_run(const void* x, int64_t x_token_stride, int64_t x_head_stride,
                    const void* weight_scale, void* out, int64_t out_row_stride, int M, int H, int weight_format,
                    int pdl, mlaqp_stream_t stream) {
   const VUpArgs a{x, x_token_stride, x_head_stride, weight, weight_scale, out, out_row_stride, M, H, weight_format};
-  return v_up_impl(a, stream, pdl != 0, kDefaultWaitLimitNs, 0);
+  return v_up_impl(a, stream, pdl, kDefaultWaitLimitNs, 0);
 }
 
 int mlaqp_debug_v_up_bounded_wait(const void* x, int64_t x_token_stride, int64_t x_head_stride, const void* weight,
@@ -995,7 +1011,7 @@ int mlaqp_debug_v_up_bounded_wait(const void* x, int64_t x_token_stride, int64_t
   if (wait_limit_ns == 0) return fail(MLAQP_ERR_INVALID_ARG, "wait_limit_ns must be > 0");
   if (extra_tx_bytes > (1u << 19)) return fail(MLAQP_ERR_INVALID_ARG, "extra_tx_bytes must be <= 2^19");
   const VUpArgs a{x, x_token_stride, x_head_stride, weight, weight_scale, out, out_row_stride, M, H, weight_format};
-  return v_up_impl(a, stream, false, wait_limit_ns, extra_tx_bytes);
+  return v_up_impl(a, stream, 0, wait_limit_ns, extra_tx_bytes);
 }
 
 int mlaqp_v_up_can_implement(int num_heads, int max_m, int weight_format, int device) {
@@ -1039,7 +1055,8 @@ int mlaqp_v_up_prewarm(int num_heads, int max_m, int weight_format, int device) 
   if (max_m >= kVLargeMinM)
     for (int ti = 0; ti < 2 && status == MLAQP_OK; ++ti) {
       cudaFuncAttributes attr;
-      e = cudaFuncGetAttributes(&attr, mlaqp::kernels_v_up_large()[weight_format][ti].fn);
+      e = cudaFuncGetAttributes(&attr, mlaqp::kernels_v_up_large()[weight_format][ti][0].fn);
+      if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, mlaqp::kernels_v_up_large()[weight_format][ti][1].fn);
       if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
     }
   if (prev != dev) cudaSetDevice(prev);

@@ -36,12 +36,14 @@ struct WarpKernelSet {
 const WarpKernelSet& kernels_warp_bf16_weights();
 const WarpKernelSet& kernels_warp_mxfp8_weights();
 
-// tcgen05 kernels for 32 < M <= 256, [nope][token tile][weight_format][out_dtype]
+// tcgen05 kernels for 32 < M <= 256, [nope][token tile][weight_format][out_dtype][early]
 // with token tiles kLargeTokTiles (tokens per CTA); the grid is
 // (tiles_per_head, H, ceil(M / token tile)) and smem_bytes the unpadded
 // layout size.
 constexpr int kLargeTokTiles[3] = {32, 64, 128};
-using LargeKernelTable = KernelInfo[2][3][2][2];
+// (early 1: the next kernel may launch at entry -- the caller's opt-in under
+// the tensor-memory contract of mlaqp_run_strided's pdl = 2).
+using LargeKernelTable = KernelInfo[2][3][2][2][2];
 const LargeKernelTable& kernels_large_m();
 
 // V up-projection kernels, [weight_format][mt-1][trig] (trig 0: at entry,
@@ -53,7 +55,7 @@ const VUpKernelTable& kernels_v_up();
 // cluster of tiles_per_head CTAs), [weight_format][token tile] with the
 // token tiles kVLargeTokTiles; grid (tiles_per_head, H, ceil(M / tile)).
 constexpr int kVLargeTokTiles[2] = {64, 128};
-using VUpLargeKernelTable = KernelInfo[2][2];
+using VUpLargeKernelTable = KernelInfo[2][2][2];  // [weight_format][token tile][early]
 const VUpLargeKernelTable& kernels_v_up_large();
 
 // Device status word of each instantiation unit (current device).

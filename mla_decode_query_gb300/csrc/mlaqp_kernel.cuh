@@ -380,6 +380,15 @@ __device__ __forceinline__ uint32_t q_off(int m, int chunk) {
   return static_cast<uint32_t>(m * (2 * K) + ((chunk ^ (m & 7)) << 4));
 }
 
+// Byte offset of 16-byte chunk `chunk` (0 or 1) of row k in a BF16 tile of
+// 16 columns (32-byte rows) as the TMA 32-byte swizzle stores it (chunk
+// index XOR bit 2 of the row): the eight rows one ldmatrix matrix reads then
+// fall into eight different bank groups.  Tile bases are multiples of 256
+// bytes (the swizzle repeats every 256).
+__device__ __forceinline__ uint32_t sw32(int k, int chunk) {
+  return static_cast<uint32_t>(32 * k + 16 * (chunk ^ ((k >> 2) & 1)));
+}
+
 // Byte offset of 16-byte chunk `chunk` of row `row` in a tile of 128-byte
 // rows stored with the TMA 128B swizzle (chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {

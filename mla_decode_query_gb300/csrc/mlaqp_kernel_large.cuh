@@ -149,11 +149,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  Grid (4, H, ceil(M/TT)); large_threads(TT) threads.
+// The kernel.  Grid (4, H, ceil(M/TT)); large_threads(TT) threads.  EARLY = 1
+// lets the next kernel launch at entry instead of after the TMEM allocation
+// (the caller's opt-in: no later kernel may take TMEM before its own
+// dependency wait, or it could hold the columns this one still needs).
 // ---------------------------------------------------------------------------
 
-template <int WF, int OD, int K, int TT>
+template <int WF, int OD, int K, int TT, int EARLY = 0>
 __global__ void __launch_bounds__(large_threads(TT)) mlaqp_fused_query_large_kernel(const __grid_constant__ RunParams p) {
+  if constexpr (EARLY) pdl_launch_dependents();
   constexpr int kLargeThreads = large_threads(TT);
   constexpr int kLargeGroups = kLargeThreads / 128;
   static_assert(K % 64 == 0 && K <= 256, "nope dim: multiple of 64, at most one TMA box (256 rows)");
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(large_threads(TT)) mlaqp_fused_query_large_ker
   // Accumulator columns in TMEM (warp 0) while the loads are in flight;
   // then the next kernel may launch.
   if (warp == 0) tmem_alloc(smem_u32(smem + L.tmem_slot), ncols);
-  pdl_launch_dependents();
+  if constexpr (!EARLY) pdl_launch_dependents();
 
   // 6. q_nope into the B tile: k slice a of row m, 16-byte chunk cc at
   //    a*TT*128 + m*128 + 16*(cc ^ m%8).

@@ -89,14 +89,6 @@ __device__ __forceinline__ int floor_div(int a, float inv) {
   return static_cast<int>(__fmaf_rn(static_cast<float>(a), inv, 0x1p-12f));
 }
 
-// Byte offset of 16-byte chunk `chunk` (0 or 1) of row k in a [K][16] BF16
-// weight tile of 32-byte rows as the TMA 32-byte swizzle stores it (chunk
-// index XOR bit 2 of the row): the eight rows one ldmatrix matrix reads then
-// fall into eight different bank groups.  Tile bases are multiples of 256
-// bytes (the swizzle repeats every 256).
-__device__ __forceinline__ uint32_t sw32(int k, int chunk) {
-  return static_cast<uint32_t>(32 * k + 16 * (chunk ^ ((k >> 2) & 1)));
-}
 
 // Epilogue of the tensor-core arm for one warp: D rows g / g+8 of MMA tile i
 // are latent columns n0+g / n0+g+8, its columns 2t, 2t+1 are tokens.  After

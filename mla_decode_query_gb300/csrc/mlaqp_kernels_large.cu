@@ -1,23 +1,28 @@
 // Instantiations of the tcgen05 query kernel for 33 <= M <= 256 (both weight
-// formats, both output dtypes, nope dims 128 and 192, 32-, 64- and 128-token CTA tiles).
+// formats, both output dtypes, nope dims 128 and 192, 32-, 64- and 128-token CTA tiles,
+// trigger after the TMEM allocation or, opted in, at entry).
 #include "mlaqp_dispatch.h"
 #include "mlaqp_kernel_large.cuh"
 
 namespace mlaqp {
 namespace {
 
-template <int K, int TT, int WF, int OD>
+template <int K, int TT, int WF, int OD, int EARLY>
 KernelInfo entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, TT>), large_threads(TT),
-                    kLargeTilesPerHead, large_smem_layout(K, TT, WF == kWeightMXFP8).bytes};
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_large_kernel<WF, OD, K, TT, EARLY>),
+                    large_threads(TT), kLargeTilesPerHead, large_smem_layout(K, TT, WF == kWeightMXFP8).bytes};
 }
 
 template <int K, int TT>
-void fill(KernelInfo (&t)[2][2]) {
-  t[kWeightBF16][kOutBF16] = entry<K, TT, kWeightBF16, kOutBF16>();
-  t[kWeightBF16][kOutE4M3] = entry<K, TT, kWeightBF16, kOutE4M3>();
-  t[kWeightMXFP8][kOutBF16] = entry<K, TT, kWeightMXFP8, kOutBF16>();
-  t[kWeightMXFP8][kOutE4M3] = entry<K, TT, kWeightMXFP8, kOutE4M3>();
+void fill(KernelInfo (&t)[2][2][2]) {
+  t[kWeightBF16][kOutBF16][0] = entry<K, TT, kWeightBF16, kOutBF16, 0>();
+  t[kWeightBF16][kOutE4M3][0] = entry<K, TT, kWeightBF16, kOutE4M3, 0>();
+  t[kWeightMXFP8][kOutBF16][0] = entry<K, TT, kWeightMXFP8, kOutBF16, 0>();
+  t[kWeightMXFP8][kOutE4M3][0] = entry<K, TT, kWeightMXFP8, kOutE4M3, 0>();
+  t[kWeightBF16][kOutBF16][1] = entry<K, TT, kWeightBF16, kOutBF16, 1>();
+  t[kWeightBF16][kOutE4M3][1] = entry<K, TT, kWeightBF16, kOutE4M3, 1>();
+  t[kWeightMXFP8][kOutBF16][1] = entry<K, TT, kWeightMXFP8, kOutBF16, 1>();
+  t[kWeightMXFP8][kOutE4M3][1] = entry<K, TT, kWeightMXFP8, kOutE4M3, 1>();
 }
 
 struct Table {

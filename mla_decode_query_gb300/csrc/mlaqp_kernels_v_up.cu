@@ -34,20 +34,24 @@ struct Table {
   }
 };
 
-template <int WF, int TT>
+template <int WF, int TT, int EARLY>
 KernelInfo large_entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_v_up_large_kernel<WF, TT>), kVLargeThreads, kVLargeSplit,
-                    v_large_smem_layout(TT, WF == kWeightMXFP8).bytes};
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_v_up_large_kernel<WF, TT, EARLY>), kVLargeThreads,
+                    kVLargeSplit, v_large_smem_layout(TT, WF == kWeightMXFP8).bytes};
 }
 
 struct LargeTable {
   VUpLargeKernelTable t;
   LargeTable() {
     static_assert(kVLargeTokTiles[0] == 64 && kVLargeTokTiles[1] == 128, "token tiles");
-    t[kWeightBF16][0] = large_entry<kWeightBF16, 64>();
-    t[kWeightBF16][1] = large_entry<kWeightBF16, 128>();
-    t[kWeightMXFP8][0] = large_entry<kWeightMXFP8, 64>();
-    t[kWeightMXFP8][1] = large_entry<kWeightMXFP8, 128>();
+    t[kWeightBF16][0][0] = large_entry<kWeightBF16, 64, 0>();
+    t[kWeightBF16][1][0] = large_entry<kWeightBF16, 128, 0>();
+    t[kWeightMXFP8][0][0] = large_entry<kWeightMXFP8, 64, 0>();
+    t[kWeightMXFP8][1][0] = large_entry<kWeightMXFP8, 128, 0>();
+    t[kWeightBF16][0][1] = large_entry<kWeightBF16, 64, 1>();
+    t[kWeightBF16][1][1] = large_entry<kWeightBF16, 128, 1>();
+    t[kWeightMXFP8][0][1] = large_entry<kWeightMXFP8, 64, 1>();
+    t[kWeightMXFP8][1][1] = large_entry<kWeightMXFP8, 128, 1>();
   }
 };
 

@@ -61,7 +61,7 @@ struct VUpParams {
 // dead once the tile is dequantised (before the dependency wait).
 template <int MT>
 struct VSmem {
-  static constexpr int W = 0;                              // BF16 [512][16], 32-byte rows
+  static constexpr int W = 0;                              // BF16 [512][16], 32-byte rows, 32B swizzle
   static constexpr int Raw = W + kLatent * kVNTile * 2;    // E4M3 [512][16]; later FP32 partials
   static constexpr int RedBytes = kVWarps * MT * 4 * 32 * 4;
   static constexpr int RawBytes = kLatent * kVNTile;
@@ -150,8 +150,7 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         o[q] = mul_bf16x2(mul_bf16x2(e4m3x2_to_bf16x2_scaled(w[q >> 1] >> (16 * (q & 1))), f1), f2);
-      *reinterpret_cast<uint4*>(smem + L::W + (j >> 1) * (kVNTile * 2) + 16 * (j & 1)) =
-          make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(smem + L::W + sw32(j >> 1, j & 1)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     __syncthreads();
   }
@@ -183,7 +182,7 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int row = 16 * (4 * warp + s) + 8 * (mi >> 1) + (lane & 7);
-    ldmatrix_x4_trans(a[s], s_w + row * (kVNTile * 2) + 16 * (mi & 1));
+    ldmatrix_x4_trans(a[s], s_w + sw32(row, mi & 1));
   }
 #pragma unroll
   for (int i = 0; i < XI; ++i) {

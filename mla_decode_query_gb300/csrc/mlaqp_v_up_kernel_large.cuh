@@ -138,8 +138,11 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t
 // The kernel.  Grid (4, H, ceil(M/TT)), cluster (4, 1, 1), 256 threads.
 // ---------------------------------------------------------------------------
 
-template <int WF, int TT>
+// EARLY = 1: the next kernel may launch at entry instead of after the TMEM
+// allocation (the caller's opt-in, as for the tcgen05 query kernel).
+template <int WF, int TT, int EARLY = 0>
 __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const __grid_constant__ VUpParams p) {
+  if constexpr (EARLY) pdl_launch_dependents();
   constexpr int K = kVLargeK;
   static_assert(TT % 16 == 0 && TT <= 128 && (TT * K / 8) % kVLargeThreads == 0, "token tile");
   constexpr VLargeSmem L = v_large_smem_layout(TT, WF == kWeightMXFP8);
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kVLargeThreads) mlaqp_v_up_large_kernel(const 
     if (m < rows) xv[i] = ld_u128(xs + m * p.x_ts + 8 * (c % KC));
   }
   if (warp == 0) tmem_alloc(smem_u32(smem + L.tmem_slot), ncols);
-  pdl_launch_dependents();
+  if constexpr (!EARLY) pdl_launch_dependents();
 
   // 6. x into the B tile: k slice j of row m, 16-byte chunk cc at
   //    j*TT*128 + m*128 + 16*(cc ^ m%8).

@@ -175,12 +175,12 @@ def mlaqp_run_strided(q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q_p
         _ptr(q_nope), int(q_nope_token_stride), int(q_nope_head_stride), _ptr(q_pe), int(q_pe_token_stride),
         int(q_pe_head_stride), _ptr(weight), _ptr(weight_scale), _ptr(out), int(out_row_stride), _ptr(q_scale),
         int(M), int(H), int(nope_dim), _fmt(weight_format, WEIGHT_FORMATS), _fmt(out_dtype, OUT_DTYPES),
-        1 if pdl else 0, _stream(stream))
+        int(pdl), _stream(stream))
 
 
 def mlaqp_prefetch_weights(weight, weight_scale, H, nope_dim, weight_format, pdl=False, stream=None) -> int:
     return load_library().mlaqp_prefetch_weights(_ptr(weight), _ptr(weight_scale), int(H), int(nope_dim),
-                                                 _fmt(weight_format, WEIGHT_FORMATS), 1 if pdl else 0,
+                                                 _fmt(weight_format, WEIGHT_FORMATS), int(pdl),
                                                  _stream(stream))
 
 
@@ -194,7 +194,7 @@ def mlaqp_debug_run_arm(q_nope, q_nope_token_stride, q_nope_head_stride, q_pe, q
         _ptr(q_nope), int(q_nope_token_stride), int(q_nope_head_stride), _ptr(q_pe), int(q_pe_token_stride),
         int(q_pe_head_stride), _ptr(weight), _ptr(weight_scale), _ptr(out), int(out_row_stride), _ptr(q_scale),
         int(M), int(H), int(nope_dim), _fmt(weight_format, WEIGHT_FORMATS), _fmt(out_dtype, OUT_DTYPES),
-        1 if pdl else 0, _fmt(arm, ARMS), _stream(stream))
+        int(pdl), _fmt(arm, ARMS), _stream(stream))
 
 
 def mlaqp_debug_set_policy(trig, cta_cap) -> int:
@@ -210,14 +210,14 @@ def mlaqp_debug_run_bounded_wait(q_nope, q_pe, weight, weight_scale, out, out_ro
 
 
 def mlaqp_debug_launch_null(ctas, threads, pdl, stream=None) -> int:
-    return load_library().mlaqp_debug_launch_null(int(ctas), int(threads), 1 if pdl else 0, _stream(stream))
+    return load_library().mlaqp_debug_launch_null(int(ctas), int(threads), int(pdl), _stream(stream))
 
 
 def mlaqp_v_up_run(x, x_token_stride, x_head_stride, weight, weight_scale, out, out_row_stride, M, H,
                    weight_format, pdl=False, stream=None) -> int:
     return load_library().mlaqp_v_up_run(_ptr(x), int(x_token_stride), int(x_head_stride), _ptr(weight),
                                          _ptr(weight_scale), _ptr(out), int(out_row_stride), int(M), int(H),
-                                         _fmt(weight_format, WEIGHT_FORMATS), 1 if pdl else 0, _stream(stream))
+                                         _fmt(weight_format, WEIGHT_FORMATS), int(pdl), _stream(stream))
 
 
 def mlaqp_v_up_can_implement(num_heads, max_m, weight_format="bf16", device=-1) -> int:

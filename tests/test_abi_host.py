@@ -213,3 +213,14 @@ def test_prefetch_validation(built_library, kw, code):
     a = dict(weight=0x1000, weight_scale=None, H=16, nope_dim=128, weight_format="bf16", stream=0)
     a.update(kw)
     assert mq.mlaqp_prefetch_weights(**a) == code, mq.mlaqp_last_error()
+
+
+def test_pdl_mode_is_validated(built_library):
+    # pdl must be 0, 1 or 2 (2: the opt-in early trigger of the tcgen05 kernels)
+    for pdl in (-1, 3):
+        st = mq.mlaqp_run_strided(0x1000, 16 * 128, 128, 0x2000, 16 * 64, 64, 0x3000, None, 0x100000, 576 * 16,
+                                  None, 4, 16, 128, "bf16", "bf16", pdl=pdl, stream=0)
+        assert st == mq.MLAQP_ERR_INVALID_ARG, (pdl, mq.mlaqp_last_error())
+        st = mq.mlaqp_v_up_run(0x1000, 16 * 512, 512, 0x3000, None, 0x100000, 128 * 16, 4, 16, "bf16", pdl=pdl,
+                               stream=0)
+        assert st == mq.MLAQP_ERR_INVALID_ARG, (pdl, mq.mlaqp_last_error())

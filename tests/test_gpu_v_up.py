@@ -136,9 +136,13 @@ def test_strided_inputs(cuda_device):
         check_bf16_region(got, acc, f"{fmt} padded view")
 
 
-def test_graph_chain_with_query_projection(cuda_device):
+@pytest.mark.parametrize("pdl", [1, 2])
+def test_graph_chain_with_query_projection(cuda_device, pdl):
     # A captured PDL chain alternating the query projection and the V
-    # up-projection on distinct layers, replayed three times.
+    # up-projection on distinct layers, replayed three times.  pdl = 2 lets
+    # the tcgen05 kernels (query above 32 tokens, V above 64) trigger the
+    # next launch at their entry: every kernel here allocates tensor memory
+    # only after its dependency wait, which is the contract that needs.
     H = 16
     Ms = (1, 8, 9, 32, 5, 16, 40, 100, 256, 3)
     steps = []
@@ -157,11 +161,12 @@ def test_graph_chain_with_query_projection(cuda_device):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for i, (M, fmt, dq, dv, tv, tq) in enumerate(steps):
-            st = mq.mlaqp_run_pdl(tq["q_nope"], tq["q_pe"], tq["weight"], tq["weight_scale"], q_outs[i], 576 * H,
-                                  None, M, H, fmt, "bf16", stream=stream)
+            st = mq.mlaqp_run_strided(tq["q_nope"], H * 128, 128, tq["q_pe"], H * 64, 64, tq["weight"],
+                                      tq["weight_scale"], q_outs[i], 576 * H, None, M, H, 128, fmt, "bf16", pdl=pdl,
+                                      stream=stream)
             assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
             st = mq.mlaqp_v_up_run(tv["x"], H * C, C, tv["weight"], tv["weight_scale"], v_outs[i], V * H, M, H,
-                                   fmt, pdl=True, stream=stream)
+                                   fmt, pdl=pdl, stream=stream)
             assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
     for _ in range(3):
         for o in q_outs + v_outs:
