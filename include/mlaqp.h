@@ -262,7 +262,7 @@ int mlaqp_debug_run_arm(const void* q_nope, int64_t q_nope_token_stride, int64_t
 
 /*
  * Measurement hook (no counterpart on the pages): overrides, process-wide,
- * the launch policy of the warp-tile kernel (M <= 32): trig = 0 lets the
+ * the launch policy of the mma.sync kernels (M <= 32): trig = 0 lets the
  * next kernel on the stream launch at kernel entry, 1 after the dependency
  * wait; cta_cap = 1..8 pads shared memory so that at most that many CTAs
  * share an SM (0: no padding).  trig = -1 restores the library's policy.

@@ -95,8 +95,6 @@ int resolve_device(int device, int* out) {
   return MLAQP_OK;
 }
 
-// Largest dynamic shared memory any launch policy below requests.
-int policy_max_smem(const DeviceInfo& d);
 // Raises every kernel's dynamic-shared-memory limit to what the launch
 // policy may request on this device (current device must be `device`).
 int setup_kernels(const DeviceInfo& d);
@@ -209,7 +207,14 @@ struct LaunchPolicy {
 // Smallest CTA cap any policy uses (the largest padded shared memory).
 constexpr int kMinCtaCap = 2;
 
+// Measurement override of the mma.sync kernels' launch policy
+// (mlaqp_debug_set_policy): trig < 0 means none.
+std::atomic<int> g_policy_trig{-1};
+std::atomic<int> g_policy_cap{0};
+
 LaunchPolicy launch_policy(int weight_format, int out_dtype, int M) {
+  const int trig = g_policy_trig.load(std::memory_order_relaxed);
+  if (trig >= 0) return LaunchPolicy{trig, g_policy_cap.load(std::memory_order_relaxed)};
   if (weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3 && M > 16) return LaunchPolicy{1, 0};
   return LaunchPolicy{0, 2};
 }
@@ -228,10 +233,6 @@ int smem_for_cap(const DeviceInfo& d, int base, int cap) {
   return bytes > base ? (bytes < d.max_smem_optin ? bytes : d.max_smem_optin) : base;
 }
 
-int policy_max_smem(const DeviceInfo& d) {
-  const int base = mlaqp::Smem<128>::Bytes > mlaqp::Smem<192>::Bytes ? mlaqp::Smem<128>::Bytes : mlaqp::Smem<192>::Bytes;
-  return smem_for_cap(d, base, kMinCtaCap);
-}
 
 // Index of a supported nope dim in the kernel tables, or -1.
 int nope_index(int K) {
@@ -329,7 +330,7 @@ int setup_kernels(const DeviceInfo& d) {
         if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
       }
   }
-  const int smem = policy_max_smem(d);
+  const int smem = smem_for_cap(d, mlaqp::Smem<192>::Bytes, 1);  // any cap the policy (or its override) uses
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
       for (int od = 0; od < 2; ++od)
@@ -431,11 +432,6 @@ const KernelInfo* lookup_warp(int weight_format, int out_dtype, int M, int trig,
   if (fma) return &set.fma[out_dtype][trig];
   return &set.mma[nope_idx][out_dtype][(M + 7) / 8 - 1][trig];
 }
-
-// Measurement override of the warp-tile launch policy (mlaqp_debug_set_policy):
-// trig < 0 means none.
-std::atomic<int> g_policy_trig{-1};
-std::atomic<int> g_policy_cap{0};
 
 // Launch policy of the warp-tile kernel: trigger at entry, at most 2 CTAs per
 // SM (with one CTA per SM per launch, a running layer and the next one each
