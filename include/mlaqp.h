@@ -192,8 +192,11 @@ int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q
  * kernels that produce q_nope / q_pe, ideally on a parallel branch (a forked
  * stream or graph branch), and not so early that other traffic evicts the
  * ~1-2 MB again.  pdl != 0 launches it with programmatic dependent launch:
- * it never waits for the previous kernel and lets the next one launch at
- * once.  Same pointer rules as mlaqp_run; no allocation, graph-capturable.
+ * it issues its fetches without waiting for the previous kernel and lets the
+ * next one launch at once; it exits only after the previous kernel has
+ * finished, so a following kernel's dependency wait still covers everything
+ * launched before it.  Same pointer rules as mlaqp_run; no allocation,
+ * graph-capturable.
  * Returns MLAQP_OK, MLAQP_ERR_UNSUPPORTED, MLAQP_ERR_INVALID_ARG or
  * MLAQP_ERR_CUDA.
  */

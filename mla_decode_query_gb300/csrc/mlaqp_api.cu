@@ -36,20 +36,28 @@ __global__ void mlaqp_null_kernel() {
 
 // L2 warm-up of one layer's weights: CTA b asks the TMA unit of its SM to
 // fetch bytes [b*chunk, (b+1)*chunk) of the weights (then the scales) into
-// L2 and exits; nothing waits for the data.  It reads only the weights, so
-// it lets the next kernel launch at once and never waits for the previous.
+// L2; nothing waits for the data.  It reads only the weights, so it lets the
+// next kernel launch at once; it still waits for the previous kernel before
+// it exits, because a later kernel's dependency wait covers only the kernel
+// launched just before it: were this one to finish first, that wait would
+// no longer imply that the kernels before it (the producer of q_nope, say)
+// have finished.
 __global__ void mlaqp_prefetch_kernel(const uint8_t* w, unsigned long long w_bytes, const uint8_t* sc,
                                       unsigned long long sc_bytes, unsigned int chunk) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x != 0) return;
-  const unsigned long long w_chunks = (w_bytes + chunk - 1) / chunk;
-  const unsigned long long b = blockIdx.x;
-  const uint8_t* base = b < w_chunks ? w : sc;
-  const unsigned long long total = b < w_chunks ? w_bytes : sc_bytes;
-  const unsigned long long off = (b < w_chunks ? b : b - w_chunks) * chunk;
-  if (off >= total) return;
-  const unsigned long long n = total - off < chunk ? total - off : chunk;
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(static_cast<unsigned>(n)) : "memory");
+  if (threadIdx.x == 0) {
+    const unsigned long long w_chunks = (w_bytes + chunk - 1) / chunk;
+    const unsigned long long b = blockIdx.x;
+    const uint8_t* base = b < w_chunks ? w : sc;
+    const unsigned long long total = b < w_chunks ? w_bytes : sc_bytes;
+    const unsigned long long off = (b < w_chunks ? b : b - w_chunks) * chunk;
+    if (off < total) {
+      const unsigned long long n = total - off < chunk ? total - off : chunk;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(static_cast<unsigned>(n))
+                   : "memory");
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 using mlaqp::KernelInfo;

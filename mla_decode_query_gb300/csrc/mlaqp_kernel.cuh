@@ -537,6 +537,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      pdl_wait();  // exit only after the previous kernel: later waits rely on it
       return;
     }
     const uint8_t* raw = smem + L::Raw;
@@ -581,6 +582,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      pdl_wait();  // exit only after the previous kernel: later waits rely on it
       return;
     }
     pdl_launch_dependents();
@@ -616,6 +618,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      pdl_wait();  // exit only after the previous kernel: later waits rely on it
       return;
     }
   }

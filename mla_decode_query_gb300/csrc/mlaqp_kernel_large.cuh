@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(large_threads(TT)) mlaqp_fused_query_large_ker
     const bool ok = mbar_wait_bounded(bar_w, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      pdl_wait();  // exit only after the previous kernel: later waits rely on it
       return;
     }
     const uint8_t* raw = smem + L.raw;

@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(32 * TS * kWMaxTilesPerCta, 2) mlaqp_query_war
   if (tid == 0) ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
   if (__syncthreads_or(!ok)) {
     if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+    pdl_wait();  // exit only after the previous kernel: later waits rely on it
     return;
   }
   if (tid != 0) ok = mbar_try_wait(s_bar, 0);  // completed: makes the tile's bytes visible to this thread

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      pdl_wait();  // exit only after the previous kernel: later waits rely on it
       return;
     }
     const uint8_t* raw = smem + L::Raw;

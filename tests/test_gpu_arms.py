@@ -218,3 +218,60 @@ def test_prefetch_weights_then_run(cuda_device, fmt, od):
     torch.cuda.synchronize()
     ref, acc = oracle.mla_query(d["q_nope"][:M], d["q_pe"][:M], d["weight"], d["weight_scale"], fmt, od, qs_val)
     check_output(_rows(out, M, H, D * H, od), ref, acc, od, f"prefetch {fmt}->{od}")
+
+
+@pytest.mark.parametrize("with_prefetch", [False, True])
+def test_dependent_chain_reads_previous_output(cuda_device, with_prefetch):
+    # Layer l+1's q_nope / q_pe are views of layer l's output (columns 0..127
+    # and 512..575 of its [M,H,576] rows), so every op depends on the one
+    # before it.  All launches are programmatic-dependent; the op triggers
+    # its successor at entry, and a weight prefetch launched in between must
+    # not break the chain (it exits only after its predecessor).  Small
+    # integers keep every layer exact: |q| <= 2 and weights in {-1, 0, 1}
+    # give |out_0| <= 256, |out_1| <= 2^15 and partial sums of layer 2 below
+    # 2^22, so the oracle's own chain must match the GPU's bit for bit.
+    H, M, L = 16, 8, 3
+    row = 576 * H
+    fmts = ["bf16", "mxfp8", "bf16"]
+    layers = [inputs.small_integer_layer(26 + l, H, M, fmts[l]) for l in range(L)]
+    dev = [_dev(d) for d in layers]
+    outs = [torch.zeros((M * row,), dtype=torch.int16, device="cuda") for _ in range(L)]
+
+    def launch_all(stream=None):
+        for l in range(L):
+            if l == 0:
+                qn, qn_ts, qn_hs, qp, qp_ts, qp_hs = dev[0]["q_nope"], H * 128, 128, dev[0]["q_pe"], H * 64, 64
+            else:
+                qn, qn_ts, qn_hs = outs[l - 1], row, 576
+                qp, qp_ts, qp_hs = outs[l - 1].data_ptr() + 2 * 512, row, 576
+            if with_prefetch:
+                assert mq.mlaqp_prefetch_weights(dev[l]["weight"], dev[l]["weight_scale"], H, 128, fmts[l], pdl=True,
+                                                 stream=stream) == mq.MLAQP_OK, mq.mlaqp_last_error()
+            st = mq.mlaqp_run_strided(qn, qn_ts, qn_hs, qp, qp_ts, qp_hs, dev[l]["weight"], dev[l]["weight_scale"],
+                                      outs[l], row, None, M, H, 128, fmts[l], "bf16", pdl=1, stream=stream)
+            assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
+
+    # The oracle's chain, from the original inputs only.
+    refs = []
+    qn, qp = layers[0]["q_nope"], layers[0]["q_pe"]
+    for l in range(L):
+        ref, acc = oracle.mla_query(qn, qp, layers[l]["weight"], layers[l]["weight_scale"], fmts[l], "bf16")
+        assert np.all(acc == np.round(acc)) and np.abs(acc).max() < 2 ** 22
+        refs.append(ref)
+        qn, qp = ref[..., :128].copy(), ref[..., 512:].copy()
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        launch_all(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch_all()
+    for rep in range(3):
+        for o in outs:
+            o.fill_(0x7FC0)  # BF16 NaN: a read of a not-yet-written output would show
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(L):
+            np.testing.assert_array_equal(_rows(outs[l], M, H, row, "bf16"), refs[l], err_msg=f"replay {rep} layer {l}")
