@@ -194,6 +194,9 @@ class LayerSet:
         return algorithmic_bytes(M, self.weight_format, self.out_dtype, self.H, self.K)
 
 
+V_MC_MIN_M = {"bf16": 9, "mxfp8": 12}
+
+
 class VLayerSet:
     """L layers of W_UV in one weight format, plus per-M attention outputs x
     and BF16 results laid out [L, M, H, *]; the V up-projection's LayerSet."""
@@ -227,7 +230,10 @@ class VLayerSet:
         return [self.x[M]]
 
     def kernel_name(self, M):
-        return "mlaqp_v_up_large_kernel" if M > 64 else "mlaqp_v_up_kernel"
+        if M > 64:
+            return "mlaqp_v_up_large_kernel"
+        # the library's switch to the x-multicast kernel (BF16 from M = 9, MXFP8 from M = 12)
+        return "mlaqp_v_up_mc_kernel" if M >= V_MC_MIN_M[self.weight_format] else "mlaqp_v_up_kernel"
 
     def launch_all(self, M, pdl=True, stream=None):
         import mla_decode_query_gb300 as mq

@@ -23,6 +23,7 @@
 #include "mlaqp_kernel_warp.cuh"
 #include "mlaqp_v_up_kernel.cuh"
 #include "mlaqp_v_up_kernel_large.cuh"
+#include "mlaqp_v_up_kernel_mc.cuh"
 
 namespace {
 
@@ -204,9 +205,10 @@ int encode_weight_map(CUtensorMap* map, const void* weight, int H, int K, bool m
 // M = 4, trigger after the wait above M = 16), MXFP8->E4M3 went from
 // 1.62 / 1.82 / 2.84 us to 1.38 / 1.52 / 2.54 us at M = 1 / 8 / 32.  The
 // exception is BF16 weights with E4M3 output above M = 16, which trigger
-// after the wait (2.16 against 2.61 us at M = 32); the V up-projection
-// likewise triggers after the wait for BF16 weights above M = 16 (2.37
-// against 2.94 us at M = 32).
+// after the wait (2.16 against 2.61 us at M = 32).  The V up-projection
+// (x-multicast kernel from M = 9) likewise triggers after the wait for BF16
+// weights at 17 <= M <= 32 (2.12 against 2.37 us at M = 32), and drops the
+// cap for MXFP8 weights above M = 32 (2.83 against 2.97 us at M = 64).
 struct LaunchPolicy {
   int trig;     // 0 entry, 1 after the wait, 2 weights ready
   int cta_cap;  // 0: none, else resident CTAs per SM
@@ -228,7 +230,7 @@ LaunchPolicy launch_policy(int weight_format, int out_dtype, int M) {
 }
 
 LaunchPolicy v_up_launch_policy(int weight_format, int M) {
-  if (M > 32) return LaunchPolicy{0, 2};  // two 32-token chunks
+  if (M > 32) return LaunchPolicy{0, weight_format == MLAQP_WEIGHT_BF16 ? 2 : 0};  // two 32-token chunks
   if (weight_format == MLAQP_WEIGHT_BF16 && M > 16) return LaunchPolicy{1, 0};
   return LaunchPolicy{0, 2};
 }
@@ -297,8 +299,12 @@ int setup_kernels(const DeviceInfo& d) {
     for (int mt = 0; mt < 4; ++mt)
       for (int trig = 0; trig < 2; ++trig) {
         const KernelInfo& k = mlaqp::kernels_v_up()[wf][mt][trig];
-        const cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   smem_for_cap(d, k.smem_bytes, kMinCtaCap));
+        cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem_for_cap(d, k.smem_bytes, kMinCtaCap));
+        if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
+        const KernelInfo& km = mlaqp::kernels_v_up_mc()[wf][mt][trig];
+        e = cudaFuncSetAttribute(km.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_for_cap(d, km.smem_bytes, kMinCtaCap));
         if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
       }
   for (int ki = 0; ki < 2; ++ki)
@@ -639,6 +645,30 @@ int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx, bo
   return MLAQP_OK;
 }
 
+// x of a V call as a 3-D tensor [M][H][512] (column fastest) for the
+// multicast kernel: box 64 columns x 1 head x tt tokens, 128-byte swizzle;
+// token rows at or beyond M read as zeros.  Returns false where the strides
+// cannot form a tensor map (the caller then uses the kernel that reads x
+// with plain loads).
+bool encode_v_x_map(CUtensorMap* map, const void* x, int64_t x_ts, int64_t x_hs, int M, int H, int tt) {
+  std::string err;
+  EncodeTiledFn fn = encode_tiled_fn(&err);
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(MLAQP_LATENT_DIM), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(M)};
+  if (x_hs <= 0) return false;
+  // The token stride of a single token is never used; any valid value does.
+  const int64_t ts = M == 1 && x_ts <= 0 ? x_hs * H : x_ts;
+  if (ts <= 0) return false;
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(x_hs) * 2, static_cast<cuuint64_t>(ts) * 2};
+  const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(tt)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Up to M = 64 the mma.sync kernel, in 32-token chunks (grid.z); above, the
 // tcgen05 cluster kernel.  Measured on GB300 (H = 16, BF16 W_UV, 128-layer
 // PDL chains, us per layer): the chunked kernel takes 3.0 / 3.0 / 5.8 / 9.4
@@ -648,6 +678,18 @@ int encode_v_weight_map(CUtensorMap* map, const void* weight, int H, bool mx, bo
 constexpr int kVLargeMinM = 65;
 
 int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }
+
+// From this M on the 8 CTAs of a (head, chunk) share x through a TMA
+// multicast.  Measured on GB300 (128-layer PDL chains, us per layer call,
+// plain loads against multicast): BF16 W_UV at H = 16 1.95 / 1.75 at M = 9,
+// 2.03 / 1.77 at M = 16; MXFP8 1.71 / 1.75 at M = 9, equal at M = 12-13,
+// 1.89 / 1.76 at M = 16.
+int v_mc_min_m(int weight_format) { return weight_format == MLAQP_WEIGHT_BF16 ? 9 : 12; }
+
+const KernelInfo* lookup_v_up_mc(int weight_format, int M, int trig) {
+  const int m = M < mlaqp::kVChunk ? M : mlaqp::kVChunk;
+  return &mlaqp::kernels_v_up_mc()[weight_format][(m + 7) / 8 - 1][trig];
+}
 
 const KernelInfo* lookup_v_up(int weight_format, int M, int trig) {
   const int m = M < mlaqp::kVChunk ? M : mlaqp::kVChunk;
@@ -720,13 +762,18 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lo
     const int tt = mlaqp::kVLargeTokTiles[v_large_tile_index(M)];
     chunks = (M + tt - 1) / tt;
     smem_bytes = tmem_safe_smem(g_dev[device], k->smem_bytes, ((M < tt ? M : tt) + 15) & ~15);
-  } else {
+  }
+  mlaqp::VUpParams params;
+  bool mc = false;
+  if (!large) {
     const LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
-    k = lookup_v_up(a.weight_format, M, pol.trig == 0 ? 0 : 1);
+    const int trig = pol.trig == 0 ? 0 : 1;
+    const int tt = 8 * (((M < mlaqp::kVChunk ? M : mlaqp::kVChunk) + 7) / 8);
+    mc = M >= v_mc_min_m(a.weight_format) && encode_v_x_map(&params.xmap, a.x, a.x_ts, a.x_hs, M, H, tt);
+    k = mc ? lookup_v_up_mc(a.weight_format, M, trig) : lookup_v_up(a.weight_format, M, trig);
     chunks = v_up_chunks(M);
     smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   }
-  mlaqp::VUpParams params;
   st = encode_v_weight_map(&params.wmap, a.weight, H, mx, large);
   if (st != MLAQP_OK) return st;
   params.x = static_cast<const uint16_t*>(a.x);
@@ -747,9 +794,9 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lo
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[2];
   unsigned n_attr = 0;
-  if (large) {  // the contraction slices of one (head, chunk) form a cluster
+  if (large || mc) {  // the CTAs of one (head, chunk) form a cluster
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
-    attr[n_attr].val.clusterDim.x = static_cast<unsigned>(mlaqp::kVLargeSplit);
+    attr[n_attr].val.clusterDim.x = static_cast<unsigned>(k->tiles_per_head);
     attr[n_attr].val.clusterDim.y = 1;
     attr[n_attr].val.clusterDim.z = 1;
     ++n_attr;
@@ -1054,6 +1101,7 @@ int mlaqp_v_up_prewarm(int num_heads, int max_m, int weight_format, int device) 
     for (int trig = 0; trig < 2 && status == MLAQP_OK; ++trig) {
       cudaFuncAttributes attr;
       e = cudaFuncGetAttributes(&attr, lookup_v_up(weight_format, 8 * mt, trig)->fn);
+      if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, lookup_v_up_mc(weight_format, 8 * mt, trig)->fn);
       if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
     }
   if (max_m >= kVLargeMinM)

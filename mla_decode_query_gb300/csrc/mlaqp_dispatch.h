@@ -51,6 +51,11 @@ const LargeKernelTable& kernels_large_m();
 using VUpKernelTable = KernelInfo[2][4][2];
 const VUpKernelTable& kernels_v_up();
 
+// V up-projection with x multicast over the 8 column-tile CTAs of a head
+// (cluster (8, 1, 1)), [weight_format][mt-1][trig], grid as kernels_v_up.
+using VUpMcKernelTable = KernelInfo[2][4][2];
+const VUpMcKernelTable& kernels_v_up_mc();
+
 // V up-projection for 64 < M <= 256 (tcgen05, contraction split over a
 // cluster of tiles_per_head CTAs), [weight_format][token tile] with the
 // token tiles kVLargeTokTiles; grid (tiles_per_head, H, ceil(M / tile)).

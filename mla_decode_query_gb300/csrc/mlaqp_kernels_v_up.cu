@@ -1,9 +1,11 @@
 // Instantiations of the V up-projection kernels: {BF16, MXFP8} W_UV x
-// ceil(M/8) in 1..4 x trigger point {entry, after the wait} for M <= 64, and
-// {BF16, MXFP8} x token tile {64, 128} of the cluster kernel above M = 64.
+// ceil(M/8) in 1..4 x trigger point {entry, after the wait} for M <= 64 (x
+// read by every CTA, and x multicast over a cluster), and {BF16, MXFP8} x
+// token tile {64, 128} of the tcgen05 cluster kernel above M = 64.
 #include "mlaqp_dispatch.h"
 #include "mlaqp_v_up_kernel.cuh"
 #include "mlaqp_v_up_kernel_large.cuh"
+#include "mlaqp_v_up_kernel_mc.cuh"
 
 namespace mlaqp {
 namespace {
@@ -25,6 +27,32 @@ void fill(KernelInfo (&t)[4][2]) {
   t[3][0] = entry<WF, 4, 0>();
   t[3][1] = entry<WF, 4, 1>();
 }
+
+template <int WF, int MT, int TRIG>
+KernelInfo mc_entry() {
+  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_v_up_mc_kernel<WF, MT, TRIG>), kVThreads, kVTilesPerHead,
+                    VMcSmem<MT>::Bytes};
+}
+
+template <int WF>
+void fill_mc(KernelInfo (&t)[4][2]) {
+  t[0][0] = mc_entry<WF, 1, 0>();
+  t[0][1] = mc_entry<WF, 1, 1>();
+  t[1][0] = mc_entry<WF, 2, 0>();
+  t[1][1] = mc_entry<WF, 2, 1>();
+  t[2][0] = mc_entry<WF, 3, 0>();
+  t[2][1] = mc_entry<WF, 3, 1>();
+  t[3][0] = mc_entry<WF, 4, 0>();
+  t[3][1] = mc_entry<WF, 4, 1>();
+}
+
+struct McTable {
+  VUpMcKernelTable t;
+  McTable() {
+    fill_mc<kWeightBF16>(t[kWeightBF16]);
+    fill_mc<kWeightMXFP8>(t[kWeightMXFP8]);
+  }
+};
 
 struct Table {
   VUpKernelTable t;
@@ -59,6 +87,11 @@ struct LargeTable {
 
 const VUpKernelTable& kernels_v_up() {
   static const Table table;
+  return table.t;
+}
+
+const VUpMcKernelTable& kernels_v_up_mc() {
+  static const McTable table;
   return table.t;
 }
 

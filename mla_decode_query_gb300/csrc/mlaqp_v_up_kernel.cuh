@@ -42,9 +42,14 @@ constexpr int kVThreads = 32 * kVWarps;               // 256
 constexpr int kVKWarp = kLatent / kVWarps;            // 64 contraction columns per warp
 constexpr int kVScaleRow = kVDim / kMxBlock;          // 4 E8M0 bytes per (h, c)
 constexpr int kVChunk = 32;                           // tokens per CTA (two grid.z chunks for 32 < M <= 64)
+// Row of the cross-warp partial-sum buffer: one warp's 32 values of one
+// (token tile, D element), padded by 4 floats so that the two 16-lane halves
+// of a summing warp (consecutive D elements) read disjoint banks.
+constexpr int kVRedRow = 36;
 
 struct VUpParams {
   CUtensorMap wmap;             // W_UV viewed as [H*512 rows][128 cols]; box 16 x 256 (64 x 128 for the cluster kernel)
+  CUtensorMap xmap;             // multicast kernel only: x as [M][H][512], box 64 x 1 x 8*MT, 128B swizzle
   const uint16_t* x;            // BF16, element (m,h,c) at m*x_ts + h*x_hs + c
   int64_t x_ts, x_hs;           // token / head strides (elements)
   const uint8_t* weight_scale;  // E8M0 [H,512,4] or null
@@ -63,7 +68,7 @@ template <int MT>
 struct VSmem {
   static constexpr int W = 0;                              // BF16 [512][16], 32-byte rows, 32B swizzle
   static constexpr int Raw = W + kLatent * kVNTile * 2;    // E4M3 [512][16]; later FP32 partials
-  static constexpr int RedBytes = kVWarps * MT * 4 * 32 * 4;
+  static constexpr int RedBytes = kVWarps * MT * 4 * kVRedRow * 4;
   static constexpr int RawBytes = kLatent * kVNTile;
   static constexpr int Scale = Raw + (RedBytes > RawBytes ? RedBytes : RawBytes);  // E8M0 [512][4]
   static constexpr int X = Scale + kLatent * kVScaleRow;   // BF16 [8*MT][512], chunks XOR-swizzled
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
     }
   }
 
-  // 7. Cross-warp sum: partial (jt, e, lane) of warp w at red[((w*MT+jt)*4+e)*32+lane].
+  // 7. Cross-warp sum: partial (jt, e, lane) of warp w at red[((w*MT+jt)*4+e)*kVRedRow+lane].
   //    D element e of lane ln is output column (ln>>2) + 8*(e>>1) and token
   //    8jt + 2*(ln&3) + (e&1); lanes ln and ln+4 hold adjacent columns.  Each
   //    thread below sums one such pair over the 8 warps, rounds it to BF16
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
 #pragma unroll
   for (int jt = 0; jt < MT; ++jt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) red[((warp * MT + jt) * 4 + e) * 32 + lane] = acc[jt][e];
+    for (int e = 0; e < 4; ++e) red[((warp * MT + jt) * 4 + e) * kVRedRow + lane] = acc[jt][e];
   __syncthreads();
   if (tid < 64 * MT) {
     const int t4 = tid & 3;           // lane & 3 of the pair
@@ -232,8 +237,8 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
     float v0 = 0.f, v1 = 0.f;
 #pragma unroll
     for (int w = 0; w < kVWarps; ++w) {
-      v0 += red[((w * MT + jt) * 4 + e) * 32 + ln];
-      v1 += red[((w * MT + jt) * 4 + e) * 32 + ln + 4];
+      v0 += red[((w * MT + jt) * 4 + e) * kVRedRow + ln];
+      v1 += red[((w * MT + jt) * 4 + e) * kVRedRow + ln + 4];
     }
     const int col = 2 * gp + 8 * (e >> 1);   // even: columns col, col+1
     const int tok = 8 * jt + 2 * t4 + (e & 1);

@@ -182,10 +182,13 @@ def test_graph_chain_with_query_projection(cuda_device, pdl):
         np.testing.assert_array_equal(qbits[..., 512:], dq["q_pe"])
 
 
-@pytest.mark.parametrize("M", [4, 100])
+@pytest.mark.parametrize("M", [4, 20, 40, 100])
 def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device, M):
-    # M = 100 runs the cluster kernel: every CTA gives up on its weight copy
-    # but still passes both cluster barriers, and no cluster writes.
+    # M = 20 and 40 run the x-multicast kernel: every CTA gives up on its
+    # weight copy but still sends its x box and waits for the others'.
+    # M = 100 runs the tcgen05 cluster kernel: every CTA gives up on its
+    # weight copy but still passes both cluster barriers, and no cluster
+    # writes.
     st, _ = mq.mlaqp_device_status(reset=True)
     assert st == mq.MLAQP_OK
     H = 8
