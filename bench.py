@@ -90,6 +90,7 @@ class LayerSet:
         self.weight_format, self.out_dtype, self.L, self.H, self.K = weight_format, out_dtype, n_layers, h, nope
         self.arm = arm
         self.pdl_mode = 1
+        self.shared_io = False  # True: every layer reads and writes the same q / out buffers
         self.m_points = tuple(m_points)
         ci = CONFIG_INDEX[weight_format] if config_index is None else config_index
         m_max = max(32, max(self.m_points))  # the first 32 token rows do not depend on m_max
@@ -148,8 +149,9 @@ class LayerSet:
         return "mlaqp_fused_query_kernel" if self.arm == "cta_mma" else "mlaqp_query_warp_kernel"
 
     def layer_args(self, M, l):
-        return dict(q_nope=self.q_nope[M][l], q_pe=self.q_pe[M][l], weight=self.weight[l],
-                    weight_scale=None if self.scale is None else self.scale[l], out=self.out[M][l],
+        io = 0 if self.shared_io else l
+        return dict(q_nope=self.q_nope[M][io], q_pe=self.q_pe[M][io], weight=self.weight[l],
+                    weight_scale=None if self.scale is None else self.scale[l], out=self.out[M][io],
                     out_row_stride=576 * self.H, q_scale=self.q_scale, M=M, H=self.H,
                     weight_format=self.weight_format, out_dtype=self.out_dtype)
 
@@ -590,6 +592,7 @@ def run_gpu(args):
         if not args.no_extras and not v_up:
             line["config0_isolated_call"] = isolated_calls(max(20, args.steps))
             line["behind_producer"] = behind_producer(max(5, args.steps), args.warmup)
+            line["workspace_reuse"] = workspace_reuse(args.sweep_steps, args.warmup)
             st = args.sweep_steps
             line["config4_sweep"] = {
                 "columns": ["pair", "H", "M", "us_per_layer", "gbs"],
@@ -651,6 +654,25 @@ def sweep(pairs, heads, m_points, steps, warmup, config_index, distinct=32):
         del base
         torch.cuda.empty_cache()
     return rows
+
+
+def workspace_reuse(steps, warmup):
+    """The headline chains (H = 16, rotated weights) with one q_nope / q_pe
+    buffer and one output workspace shared by every layer, as in a decode
+    step, where the producer has just written q and attention reads the
+    output next.  The headline `points` rotate q and out with the weights."""
+    rows = []
+    for fmt, od in FORMATS:
+        ls = LayerSet(fmt, od, layers_for(fmt, H), m_points=M_POINTS, distinct=32)
+        ls.shared_io = True
+        for M in M_POINTS:
+            g = ls.capture(M)
+            us = time_graph(g, ls.L, steps, warmup)
+            rows.append([f"{fmt}->{od}", M, round(us, 4), round(ls.bytes_per_call(M) / (us * 1e-6) / 1e9, 1)])
+            del g
+        del ls
+    return {"columns": ["pair", "M", "us_per_layer", "gbs"], "rows": rows,
+            "note": "weights rotated as in the headline; q and out shared by all layers (a reused workspace)"}
 
 
 def isolated_calls(steps):
