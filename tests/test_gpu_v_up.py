@@ -245,3 +245,52 @@ def test_larger_token_counts_bit_exact(cuda_device):
         for M in (64, 100, 256):
             got = _rows(_run(t, M, 16, fmt), M, 16, V * 16)
             np.testing.assert_array_equal(got, ref[:M], err_msg=f"{fmt} M{M}")
+
+
+@pytest.mark.parametrize("M,qfmt,vfmt", [(20, "bf16", "mxfp8"), (40, "mxfp8", "bf16"), (5, "bf16", "bf16")])
+def test_reads_x_written_by_the_previous_kernel(cuda_device, M, qfmt, vfmt):
+    # A PDL chain in which the V up-projection's x is the query op's output
+    # (columns 0..511 of its [M,H,576] rows, head stride 576), so the V
+    # kernel reads data the kernel just before it wrote: at M = 20 and 40
+    # through the x multicast (a TMA copy after the dependency wait), at
+    # M = 5 through plain loads.  Small integers keep both steps exact
+    # (|projection| <= 256, V partial sums <= 2^17), so the oracle's own
+    # chain must match bit for bit.  Outputs start as BF16 NaN each replay.
+    H = 16
+    row = 576 * H
+    dq = inputs.small_integer_layer(60 + M, H, M, qfmt)
+    dv = inputs.small_integer_v_layer(61 + M, H, M, vfmt)
+    tq = dict(q_nope=to_device(dq["q_nope"]), q_pe=to_device(dq["q_pe"]), weight=to_device(dq["weight"]),
+              weight_scale=None if dq["weight_scale"] is None else to_device(dq["weight_scale"]))
+    tv = _dev(dv)
+    q_out = torch.zeros((M * row,), dtype=torch.int16, device="cuda")
+    v_out = torch.zeros((M * V * H,), dtype=torch.int16, device="cuda")
+
+    def launch(stream=None):
+        st = mq.mlaqp_run_strided(tq["q_nope"], H * 128, 128, tq["q_pe"], H * 64, 64, tq["weight"], tq["weight_scale"],
+                                  q_out, row, None, M, H, 128, qfmt, "bf16", pdl=1, stream=stream)
+        assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
+        st = mq.mlaqp_v_up_run(q_out, row, 576, tv["weight"], tv["weight_scale"], v_out, V * H, M, H, vfmt, pdl=1,
+                               stream=stream)
+        assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
+
+    qref, qacc = oracle.mla_query(dq["q_nope"], dq["q_pe"], dq["weight"], dq["weight_scale"], qfmt, "bf16")
+    assert np.all(qacc == np.round(qacc)) and np.abs(qacc).max() <= 256
+    vref, vacc = oracle.mla_v_up(np.ascontiguousarray(qref[..., :C]), dv["weight"], dv["weight_scale"], vfmt)
+    assert np.all(vacc == np.round(vacc)) and np.abs(vacc).max() <= 2 ** 17
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        launch(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch()
+    for rep in range(3):
+        q_out.fill_(0x7FC0)
+        v_out.fill_(0x7FC0)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_host_bits(q_out, np.uint16).reshape(M, H, 576), qref, err_msg=f"query {rep}")
+        np.testing.assert_array_equal(_rows(v_out, M, H, V * H), vref, err_msg=f"v_up {rep}")
