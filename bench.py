@@ -140,12 +140,15 @@ class LayerSet:
         return [self.q_nope[M], self.q_pe[M]]
 
     def kernel_name(self, M):
-        if self.arm == "tcgen05" or (self.arm == "auto" and M > 32):
+        if self.arm == "tcgen05":
             return "mlaqp_fused_query_large_kernel"
         if self.arm == "auto":
             import mla_decode_query_gb300 as mq
             st, grid, _ = mq.mlaqp_launch_shape(M, self.H, self.weight_format, self.out_dtype)
-            return "mlaqp_fused_query_kernel" if st == 0 and grid == 8 * self.H else "mlaqp_query_warp_kernel"
+            cta = st == 0 and grid == 8 * self.H * -(-M // 32)  # the CTA-tile kernel, one CTA per 32-token chunk
+            if M > 32:
+                return "mlaqp_fused_query_kernel" if cta else "mlaqp_fused_query_large_kernel"
+            return "mlaqp_fused_query_kernel" if cta else "mlaqp_query_warp_kernel"
         return "mlaqp_fused_query_kernel" if self.arm == "cta_mma" else "mlaqp_query_warp_kernel"
 
     def layer_args(self, M, l):

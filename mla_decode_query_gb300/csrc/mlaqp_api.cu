@@ -225,7 +225,7 @@ std::atomic<int> g_policy_cap{0};
 LaunchPolicy launch_policy(int weight_format, int out_dtype, int M) {
   const int trig = g_policy_trig.load(std::memory_order_relaxed);
   if (trig >= 0) return LaunchPolicy{trig, g_policy_cap.load(std::memory_order_relaxed)};
-  if (weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3 && M > 16) return LaunchPolicy{1, 0};
+  if (weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3 && M > 16 && M <= 32) return LaunchPolicy{1, 0};
   return LaunchPolicy{0, 2};
 }
 
@@ -251,8 +251,20 @@ int nope_index(int K) {
   return -1;
 }
 
+// From M = 33 to this M the CTA-tile kernel runs in 32-token chunks
+// (grid.z = 2; the second chunk finds the weight tile in L2) instead of the
+// tcgen05 kernel.  It needs no tensor memory, so it may trigger the next
+// launch at entry.  Measured on GB300 (128/256-layer PDL chains, pdl = 1, us
+// per layer call, H = 16, tcgen05 / chunked): BF16->BF16 2.43 / 2.08 at
+// M = 33 and 2.51 / 2.28 at 64; MXFP8->E4M3 3.22 / 2.43 and 3.34 / 2.52;
+// BF16->E4M3 2.46 / 2.12 and 2.55 / 2.27 (entry trigger, cap 2; after-wait
+// trigger 2.68 / 2.74).
+constexpr int kCtaMaxM = 64;
+
+int cta_chunks(int M) { return (M + mlaqp::kMaxM - 1) / mlaqp::kMaxM; }
+
 const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int nope_idx) {
-  const int mt = (M + 7) / 8;
+  const int mt = ((M < mlaqp::kMaxM ? M : mlaqp::kMaxM) + 7) / 8;
   if (mt < 1 || mt > 4) return nullptr;
   const mlaqp::KernelTable& table =
       weight_format == MLAQP_WEIGHT_BF16 ? mlaqp::kernels_bf16_weights() : mlaqp::kernels_mxfp8_weights();
@@ -422,7 +434,7 @@ int warp_crossover(int weight_format, int out_dtype, int H) {
 }
 
 Arm auto_arm(int weight_format, int out_dtype, int M, int H, int K) {
-  if (M > MLAQP_MAX_M_DECODE) return Arm::kTcgen05;
+  if (M > MLAQP_MAX_M_DECODE) return M <= kCtaMaxM ? Arm::kCtaMma : Arm::kTcgen05;
   if (M < warp_crossover(weight_format, out_dtype, H)) return Arm::kCtaMma;
   if (K != MLAQP_NOPE_DIM && M > 24 && !(weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3))
     return Arm::kCtaMma;
@@ -566,8 +578,9 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
   if (arm == Arm::kAuto) arm = auto_arm(a.weight_format, a.out_dtype, M, H, K);
   if (arm == Arm::kWarpFma && (M > 8 || K != 128))
     return fail(MLAQP_ERR_UNSUPPORTED, "the CUDA-core arm covers M <= 8 at nope_dim 128");
-  if ((arm == Arm::kWarpMma || arm == Arm::kCtaMma) && M > MLAQP_MAX_M_DECODE)
-    return fail(MLAQP_ERR_UNSUPPORTED, "the mma.sync arms cover M <= 32");
+  if (arm == Arm::kWarpMma && M > MLAQP_MAX_M_DECODE)
+    return fail(MLAQP_ERR_UNSUPPORTED, "the warp-tile arm covers M <= 32");
+  if (arm == Arm::kCtaMma && M > kCtaMaxM) return fail(MLAQP_ERR_UNSUPPORTED, "the CTA-tile arm covers M <= 64");
   if (arm == Arm::kWarpMma || arm == Arm::kWarpFma) return launch_warp(a, stream, pdl, wait_limit_ns, extra_tx, arm, device);
 
   const bool large = arm == Arm::kTcgen05;
@@ -601,7 +614,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H),
-                     static_cast<unsigned>(large ? large_chunks(M) : 1));
+                     static_cast<unsigned>(large ? large_chunks(M) : cta_chunks(M)));
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -916,15 +929,16 @@ int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q
 int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas, int* threads_per_cta) {
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
-  if (M > MLAQP_MAX_M_DECODE) {
+  const Arm arm = auto_arm(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM);
+  if (arm == Arm::kTcgen05) {
     const KernelInfo* k = lookup_large(weight_format, out_dtype, 0, large_tile_index(M));
     if (grid_ctas) *grid_ctas = k->tiles_per_head * H * large_chunks(M);
     if (threads_per_cta) *threads_per_cta = k->threads;
     return MLAQP_OK;
   }
-  if (auto_arm(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM) == Arm::kCtaMma) {
+  if (arm == Arm::kCtaMma) {
     const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0);
-    if (grid_ctas) *grid_ctas = k->tiles_per_head * H;
+    if (grid_ctas) *grid_ctas = k->tiles_per_head * H * cta_chunks(M);
     if (threads_per_cta) *threads_per_cta = k->threads;
     return MLAQP_OK;
   }

@@ -406,8 +406,8 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // one 4-byte store.
 template <int OD, int MTW, int TS, int MODE>
 __device__ __forceinline__ void write_projection(const RunParams& p, const float (&acc)[MTW][4], int wcol, int wtok,
-                                                 int lane, int h, int n_cta, const uint32_t* divtab, float qs,
-                                                 float rcp) {
+                                                 int lane, int h, int n_cta, int m0, int M, const uint32_t* divtab,
+                                                 float qs, float rcp) {
   constexpr int MT = MTW;  // this warp's token tiles: jt = wtok + TS*i, i < MTW
   const int g = lane >> 2;
   const int t = lane & 3;
@@ -437,10 +437,10 @@ __device__ __forceinline__ void write_projection(const RunParams& p, const float
   }
 #pragma unroll
   for (int jt = 0; jt < MT; ++jt) {
-    const int m = 8 * (wtok + TS * jt) + g;  // beyond the last tile m >= M: no store
-    if (m < p.M) {
-      const size_t off =
-          static_cast<size_t>(m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + n_cta + 16 * wcol + 2 * t;
+    const int m = 8 * (wtok + TS * jt) + g;  // token of the chunk; beyond the last tile m >= M: no store
+    if (m < M) {
+      const size_t off = static_cast<size_t>(m0 + m) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + n_cta +
+                         16 * wcol + 2 * t;
       if constexpr (OD == kOutBF16) {
         uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + off;
         *reinterpret_cast<uint32_t*>(o) = r[jt][0];
@@ -493,8 +493,11 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   const int lane = tid & 31;
   const int wcol = warp & (kWarps - 1);  // 16-column MMA tile of this warp
   const int wtok = warp / kWarps;        // token group of this warp
-  const int M = p.M;
+  const int m0 = blockIdx.z * kMaxM;        // this CTA's tokens: [m0, m0 + M)
+  const int M = min(kMaxM, p.M - m0);      // >= 1: the grid has ceil(M / 32) token chunks
   const int n_cta = tile * kNTile;
+  const uint16_t* const q_nope = p.q_nope + m0 * p.q_nope_ts;
+  const uint16_t* const q_pe = p.q_pe + m0 * p.q_pe_ts;
 
   // The next kernel on the stream may start its independent prologue.
   if constexpr (TRIG == 0) pdl_launch_dependents();
@@ -524,10 +527,10 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   //    fetched before the producer writes it is updated by that write; the
   //    values themselves are read only after the dependency wait).
   if (warp == 0 && lane < M) {
-    const uint16_t* qrow = p.q_nope + lane * p.q_nope_ts + h * p.q_nope_hs;
+    const uint16_t* qrow = q_nope + lane * p.q_nope_ts + h * p.q_nope_hs;
 #pragma unroll
     for (int o = 0; o < K; o += 64) prefetch_l2(qrow + o);
-    prefetch_l2(p.q_pe + lane * p.q_pe_ts + h * p.q_pe_hs);
+    prefetch_l2(q_pe + lane * p.q_pe_ts + h * p.q_pe_hs);
   }
   __syncthreads();  // barrier initialised before anyone waits on it
 
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   const bool has_pe = j_pe < M * (kRope / 2);
   const int m_pe = j_pe >> 5;
   uint32_t pe = 0u;
-  if (has_pe) pe = ld_u32(p.q_pe + m_pe * p.q_pe_ts + h * p.q_pe_hs + 2 * (j_pe & 31));
+  if (has_pe) pe = ld_u32(q_pe + m_pe * p.q_pe_ts + h * p.q_pe_hs + 2 * (j_pe & 31));
   constexpr int kQChunks = 8 * MT * KC;  // 16-byte chunks of the [8*MT][K] tile
   constexpr int QI = (kQChunks + kCta - 1) / kCta;
   uint4 qv[QI];
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     const int c = tid + kCta * i;  // chunk c: token row c/KC, k chunk c%KC
     const int m = c / KC;
     qv[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (c < kQChunks && m < M) qv[i] = ld_u128(p.q_nope + m * p.q_nope_ts + h * p.q_nope_hs + 8 * (c % KC));
+    if (c < kQChunks && m < M) qv[i] = ld_u128(q_nope + m * p.q_nope_ts + h * p.q_nope_hs + 8 * (c % KC));
   }
 
   if constexpr (WF == kWeightMXFP8) {
@@ -665,7 +668,7 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
 
   // 8. (ahead of the contraction, overlapping its latency) the q_pe append.
   if (has_pe) {
-    const size_t off = static_cast<size_t>(m_pe) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + kLatent +
+    const size_t off = static_cast<size_t>(m0 + m_pe) * p.out_row_stride + static_cast<size_t>(h) * kOutDim + kLatent +
                        2 * (j_pe & 31);
     if (OD == kOutBF16 || mul_ok) {
       write_pe_pair<OD, kE4m3MulExact>(p, off, pe, divtab, qs, rcp);
@@ -708,13 +711,13 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   // 7. Epilogue; the E4M3 division form is chosen once per CTA so that the
   //    common path holds no call and no branch.
   if constexpr (OD == kOutBF16) {
-    write_projection<OD, MTW, TS, kE4m3MulExact>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
+    write_projection<OD, MTW, TS, kE4m3MulExact>(p, acc[0], wcol, wtok, lane, h, n_cta, m0, M, divtab, qs, rcp);
   } else if (mul_ok) {
-    write_projection<OD, MTW, TS, kE4m3MulExact>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
+    write_projection<OD, MTW, TS, kE4m3MulExact>(p, acc[0], wcol, wtok, lane, h, n_cta, m0, M, divtab, qs, rcp);
   } else if (table_ok) {
-    write_projection<OD, MTW, TS, kE4m3Table>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
+    write_projection<OD, MTW, TS, kE4m3Table>(p, acc[0], wcol, wtok, lane, h, n_cta, m0, M, divtab, qs, rcp);
   } else {
-    write_projection<OD, MTW, TS, kE4m3Divide>(p, acc[0], wcol, wtok, lane, h, n_cta, divtab, qs, rcp);
+    write_projection<OD, MTW, TS, kE4m3Divide>(p, acc[0], wcol, wtok, lane, h, n_cta, m0, M, divtab, qs, rcp);
   }
 }
 

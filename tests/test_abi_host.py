@@ -105,11 +105,13 @@ def test_launch_shape(built_library):
         for m in (1, 5, 8):
             st, grid, threads = mq.mlaqp_launch_shape(m, h, "mxfp8", "e4m3")
             assert st == mq.MLAQP_OK and grid == 8 * h and threads == 128
-    # Above M = 32: the tcgen05 kernel, 4 CTAs per head and token chunk (32
-    # tokens up to M = 64, 64 up to 128, then 128), 256 threads (512 for the
-    # 64- and 128-token chunks)
-    for m, chunks, thr in ((33, 2, 256), (64, 2, 256), (65, 2, 512), (128, 2, 512), (129, 2, 512),
-                           (200, 2, 512), (256, 2, 512)):
+    # M = 33..64: the CTA-tile kernel in two 32-token chunks (grid.z), two
+    # token groups.  Above M = 64: the tcgen05 kernel, 4 CTAs per head and
+    # token chunk (64 tokens up to M = 128, then 128), 512 threads.
+    for m in (33, 64):
+        st, grid, threads = mq.mlaqp_launch_shape(m, 11, "bf16", "bf16")
+        assert st == mq.MLAQP_OK and grid == 8 * 11 * 2 and threads == 256
+    for m, chunks, thr in ((65, 2, 512), (128, 2, 512), (129, 2, 512), (200, 2, 512), (256, 2, 512)):
         st, grid, threads = mq.mlaqp_launch_shape(m, 11, "bf16", "bf16")
         assert st == mq.MLAQP_OK and grid == 4 * 11 * chunks and threads == thr
     assert mq.mlaqp_launch_shape(0, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED

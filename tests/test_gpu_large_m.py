@@ -1,6 +1,7 @@
 """GPU parity of the larger token counts, 33 <= M <= 256 (multi-token
-prediction and prefill-sized steps; the tcgen05 / TMEM kernel), against the
-CPU oracle through the C ABI.
+prediction and prefill-sized steps; up to M = 64 the CTA-tile kernel in
+32-token chunks, above that the tcgen05 / TMEM kernel), against the CPU
+oracle through the C ABI.
 
 Tokens are independent rows of the operation, so one oracle evaluation at
 M = 256 serves every smaller M of the same layer (its first M rows).
@@ -59,6 +60,9 @@ def test_domain_and_launch_shape(cuda_device):
     assert mq.mlaqp_can_implement(16, M_MAX + 1) == 0
     st, grid, threads = mq.mlaqp_launch_shape(200, 16, "bf16", "bf16")
     assert st == mq.MLAQP_OK and grid == 4 * 16 * 2 and threads == 512
+    for fmt, od in PAIRS:  # 33..64: the CTA-tile kernel, two 32-token chunks
+        st, grid, threads = mq.mlaqp_launch_shape(40, 16, fmt, od)
+        assert st == mq.MLAQP_OK and grid == 8 * 16 * 2 and threads == 256
 
 
 @pytest.mark.parametrize("fmt,od", PAIRS)
@@ -183,13 +187,15 @@ def test_graph_chain_mixed_token_counts(cuda_device):
         check_output(_rows(outs[i], M, H, D * H, od), ref, acc, od, f"graph layer {i} {fmt}->{od} M{M}")
 
 
-def test_bounded_wait_reports_timeout_and_frees_tmem(cuda_device):
+@pytest.mark.parametrize("M", [64, 100])
+def test_bounded_wait_reports_timeout_and_frees_tmem(cuda_device, M):
     # Every CTA's weight wait runs out (2 ms): the kernel records the timeout,
-    # releases its tensor memory, writes nothing; later runs (which allocate
-    # tensor memory again on the same SMs) still work.
+    # writes nothing, and (M = 100, the tcgen05 kernel) releases its tensor
+    # memory; later runs (which allocate tensor memory again on the same SMs)
+    # still work.  M = 64 runs the CTA-tile kernel in two chunks.
     st, _ = mq.mlaqp_device_status(reset=True)
     assert st == mq.MLAQP_OK
-    H, M = 8, 64
+    H = 8
     for fmt in ("bf16", "mxfp8"):
         d = inputs.make_layer(36, H, fmt, m_max=M)
         t = _dev(d)

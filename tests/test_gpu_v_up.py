@@ -140,7 +140,7 @@ def test_strided_inputs(cuda_device):
 def test_graph_chain_with_query_projection(cuda_device, pdl):
     # A captured PDL chain alternating the query projection and the V
     # up-projection on distinct layers, replayed three times.  pdl = 2 lets
-    # the tcgen05 kernels (query above 32 tokens, V above 64) trigger the
+    # the tcgen05 kernels (query and V above 64 tokens) trigger the
     # next launch at their entry: every kernel here allocates tensor memory
     # only after its dependency wait, which is the contract that needs.
     H = 16
