@@ -26,9 +26,10 @@
  *     on an sm_103 (GB300) device.  M <= 32 is the decode domain of the
  *     pages; 33..256 extends it to the multi-token-prediction and
  *     prefill-sized steps that the pages leave to the staged BMM (vLLM PR
- *     #174, sections Safety scope and E2E topology matrix): up to M = 64
- *     the decode (mma.sync) kernel runs in 32-token chunks, above that a
- *     tcgen05 (TMEM-accumulator) kernel takes its place.
+ *     #174, sections Safety scope and E2E topology matrix): the decode
+ *     (mma.sync) kernel runs in 32-token chunks up to M = 64, and up to
+ *     M = 128 while its 8*H*ceil(M/32) CTAs fit the device at two per SM;
+ *     beyond that a tcgen05 (TMEM-accumulator) kernel takes its place.
  *   - Status codes are the mlaqp_status values; on any non-OK status a
  *     message is available from mlaqp_last_error() on the same thread.
  *
@@ -163,8 +164,8 @@ int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
  * (BF16 or E4M3) and weight_scale [H, nope_dim, 16]; everything else is as
  * for mlaqp_run.
  *
- * pdl = 2 (opt-in, no counterpart on the pages): as pdl = 1, and for
- * M > 64 the tcgen05 kernel lets the next kernel on the stream launch at
+ * pdl = 2 (opt-in, no counterpart on the pages): as pdl = 1, and where the
+ * call runs the tcgen05 kernel it lets the next kernel on the stream launch at
  * its entry rather than after it has allocated tensor memory (about 0.5 us
  * less per layer call in a chain).  The caller promises the tensor-memory
  * contract this needs: no kernel launched after this call on `stream`, while
@@ -172,8 +173,8 @@ int mlaqp_run_pdl(const void* q_nope, const void* q_pe, const void* weight,
  * its own dependency wait -- otherwise such a kernel could hold the columns
  * this call is waiting for while it waits for this call, and neither would
  * finish.  Every kernel of this library allocates tensor memory only after
- * its dependency wait, so chains of its calls meet the contract.  For
- * M <= 64, pdl = 2 is pdl = 1.  Other values return MLAQP_ERR_INVALID_ARG.
+ * its dependency wait, so chains of its calls meet the contract.  For the
+ * mma.sync kernels, pdl = 2 is pdl = 1.  Other values return MLAQP_ERR_INVALID_ARG.
  */
 int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q_nope_head_stride,
                       const void* q_pe, int64_t q_pe_token_stride, int64_t q_pe_head_stride,
@@ -247,7 +248,7 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
  *                       cores with a warp-shuffle reduction (M <= 8,
  *                       nope_dim 128)
  *   MLAQP_ARM_CTA_MMA   the CTA-tile mma.sync kernel (64 latent columns per
- *                       CTA, q_nope staged in shared memory; M <= 64, in
+ *                       CTA, q_nope staged in shared memory; M <= 128, in
  *                       32-token chunks above 32)
  *   MLAQP_ARM_TCGEN05   the tcgen05 kernel (TMEM accumulator; any M)
  * A form that does not cover the call returns MLAQP_ERR_UNSUPPORTED; every
@@ -267,7 +268,7 @@ int mlaqp_debug_run_arm(const void* q_nope, int64_t q_nope_token_stride, int64_t
 
 /*
  * Measurement hook (no counterpart on the pages): overrides, process-wide,
- * the launch policy of the mma.sync kernels (M <= 64): trig = 0 lets the
+ * the launch policy of the mma.sync kernels: trig = 0 lets the
  * next kernel on the stream launch at kernel entry, 1 after the dependency
  * wait; cta_cap = 1..8 pads shared memory so that at most that many CTAs
  * share an SM (0: no padding).  trig = -1 restores the library's policy.

@@ -251,17 +251,26 @@ int nope_index(int K) {
   return -1;
 }
 
-// From M = 33 to this M the CTA-tile kernel runs in 32-token chunks
-// (grid.z = 2; the second chunk finds the weight tile in L2) instead of the
-// tcgen05 kernel.  It needs no tensor memory, so it may trigger the next
+// Above M = 32 the CTA-tile kernel runs in 32-token chunks (grid.z; the
+// later chunks find the weight tile in L2) instead of the tcgen05 kernel:
+// always up to M = 64, and up to kCtaMaxM while all its CTAs fit on the GPU
+// at two per SM.  It needs no tensor memory, so it may trigger the next
 // launch at entry.  Measured on GB300 (128/256-layer PDL chains, pdl = 1, us
-// per layer call, H = 16, tcgen05 / chunked): BF16->BF16 2.43 / 2.08 at
+// per layer call, tcgen05 / chunked): H = 16, BF16->BF16 2.43 / 2.08 at
 // M = 33 and 2.51 / 2.28 at 64; MXFP8->E4M3 3.22 / 2.43 and 3.34 / 2.52;
 // BF16->E4M3 2.46 / 2.12 and 2.55 / 2.27 (entry trigger, cap 2; after-wait
-// trigger 2.68 / 2.74).
-constexpr int kCtaMaxM = 64;
+// trigger 2.68 / 2.74).  H = 8 (four chunks, 256 CTAs), M = 128: BF16->BF16
+// 2.83 / 2.09, MXFP8->E4M3 3.27 / 2.39.  H = 16 with three or four chunks
+// (384-512 CTAs, more than fit): 3.6-4.7 against 2.8-3.5.
+constexpr int kCtaMaxM = 128;
+constexpr int kCtaAlwaysM = 64;
 
 int cta_chunks(int M) { return (M + mlaqp::kMaxM - 1) / mlaqp::kMaxM; }
+
+bool cta_chunks_fit(int M, int H, int sm_count) {
+  if (M <= kCtaAlwaysM) return true;
+  return M <= kCtaMaxM && mlaqp::kTilesPerHead * H * cta_chunks(M) <= 2 * sm_count;
+}
 
 const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int nope_idx) {
   const int mt = ((M < mlaqp::kMaxM ? M : mlaqp::kMaxM) + 7) / 8;
@@ -433,8 +442,9 @@ int warp_crossover(int weight_format, int out_dtype, int H) {
   return out_dtype == MLAQP_OUT_BF16 ? 13 : 16;
 }
 
-Arm auto_arm(int weight_format, int out_dtype, int M, int H, int K) {
-  if (M > MLAQP_MAX_M_DECODE) return M <= kCtaMaxM ? Arm::kCtaMma : Arm::kTcgen05;
+// sm_count is read only above M = kCtaAlwaysM.
+Arm auto_arm(int weight_format, int out_dtype, int M, int H, int K, int sm_count) {
+  if (M > MLAQP_MAX_M_DECODE) return cta_chunks_fit(M, H, sm_count) ? Arm::kCtaMma : Arm::kTcgen05;
   if (M < warp_crossover(weight_format, out_dtype, H)) return Arm::kCtaMma;
   if (K != MLAQP_NOPE_DIM && M > 24 && !(weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3))
     return Arm::kCtaMma;
@@ -575,12 +585,12 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
   if (st != MLAQP_OK) return st;
 
   Arm arm = forced;
-  if (arm == Arm::kAuto) arm = auto_arm(a.weight_format, a.out_dtype, M, H, K);
+  if (arm == Arm::kAuto) arm = auto_arm(a.weight_format, a.out_dtype, M, H, K, g_dev[device].sm_count);
   if (arm == Arm::kWarpFma && (M > 8 || K != 128))
     return fail(MLAQP_ERR_UNSUPPORTED, "the CUDA-core arm covers M <= 8 at nope_dim 128");
   if (arm == Arm::kWarpMma && M > MLAQP_MAX_M_DECODE)
     return fail(MLAQP_ERR_UNSUPPORTED, "the warp-tile arm covers M <= 32");
-  if (arm == Arm::kCtaMma && M > kCtaMaxM) return fail(MLAQP_ERR_UNSUPPORTED, "the CTA-tile arm covers M <= 64");
+  if (arm == Arm::kCtaMma && M > kCtaMaxM) return fail(MLAQP_ERR_UNSUPPORTED, "the CTA-tile arm covers M <= 128");
   if (arm == Arm::kWarpMma || arm == Arm::kWarpFma) return launch_warp(a, stream, pdl, wait_limit_ns, extra_tx, arm, device);
 
   const bool large = arm == Arm::kTcgen05;
@@ -929,7 +939,16 @@ int mlaqp_run_strided(const void* q_nope, int64_t q_nope_token_stride, int64_t q
 int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas, int* threads_per_cta) {
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
-  const Arm arm = auto_arm(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM);
+  int sm_count = 0;
+  if (M > kCtaAlwaysM) {  // the choice depends on the device's SM count
+    int dev = 0;
+    int st = resolve_device(-1, &dev);
+    if (st != MLAQP_OK) return st;
+    st = check_device(dev);
+    if (st != MLAQP_OK) return st;
+    sm_count = g_dev[dev].sm_count;
+  }
+  const Arm arm = auto_arm(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM, sm_count);
   if (arm == Arm::kTcgen05) {
     const KernelInfo* k = lookup_large(weight_format, out_dtype, 0, large_tile_index(M));
     if (grid_ctas) *grid_ctas = k->tiles_per_head * H * large_chunks(M);

@@ -106,14 +106,11 @@ def test_launch_shape(built_library):
             st, grid, threads = mq.mlaqp_launch_shape(m, h, "mxfp8", "e4m3")
             assert st == mq.MLAQP_OK and grid == 8 * h and threads == 128
     # M = 33..64: the CTA-tile kernel in two 32-token chunks (grid.z), two
-    # token groups.  Above M = 64: the tcgen05 kernel, 4 CTAs per head and
-    # token chunk (64 tokens up to M = 128, then 128), 512 threads.
+    # token groups.  Above M = 64 the choice depends on the device's SM count
+    # (checked on the GPU).
     for m in (33, 64):
         st, grid, threads = mq.mlaqp_launch_shape(m, 11, "bf16", "bf16")
         assert st == mq.MLAQP_OK and grid == 8 * 11 * 2 and threads == 256
-    for m, chunks, thr in ((65, 2, 512), (128, 2, 512), (129, 2, 512), (200, 2, 512), (256, 2, 512)):
-        st, grid, threads = mq.mlaqp_launch_shape(m, 11, "bf16", "bf16")
-        assert st == mq.MLAQP_OK and grid == 4 * 11 * chunks and threads == thr
     assert mq.mlaqp_launch_shape(0, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(257, 16)[0] == mq.MLAQP_ERR_UNSUPPORTED
     assert mq.mlaqp_launch_shape(4, 12)[0] == mq.MLAQP_ERR_UNSUPPORTED

@@ -58,11 +58,22 @@ def test_domain_and_launch_shape(cuda_device):
             assert mq.mlaqp_can_implement(h, M_MAX, weight_format=fmt, out_dtype=od) == 1, mq.mlaqp_last_error()
             assert mq.mlaqp_prewarm(h, M_MAX, fmt, od) == mq.MLAQP_OK, mq.mlaqp_last_error()
     assert mq.mlaqp_can_implement(16, M_MAX + 1) == 0
-    st, grid, threads = mq.mlaqp_launch_shape(200, 16, "bf16", "bf16")
-    assert st == mq.MLAQP_OK and grid == 4 * 16 * 2 and threads == 512
-    for fmt, od in PAIRS:  # 33..64: the CTA-tile kernel, two 32-token chunks
-        st, grid, threads = mq.mlaqp_launch_shape(40, 16, fmt, od)
-        assert st == mq.MLAQP_OK and grid == 8 * 16 * 2 and threads == 256
+    # Above M = 32 the CTA-tile kernel in 32-token chunks (256 threads): up to
+    # M = 64 always, up to 128 while its 8*H*chunks CTAs fit at two per SM;
+    # otherwise the tcgen05 kernel, 4 CTAs per head and token chunk (32 tokens
+    # up to M = 64, 64 up to 128, then 128), 512 threads from 64-token chunks.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for fmt, od in PAIRS:
+        for h in (8, 11, 16):
+            for m in (33, 40, 64, 65, 96, 97, 128, 129, 200, 256):
+                st, grid, threads = mq.mlaqp_launch_shape(m, h, fmt, od)
+                assert st == mq.MLAQP_OK
+                chunks = -(-m // 32)
+                if m <= 64 or (m <= 128 and 8 * h * chunks <= 2 * sms):
+                    assert grid == 8 * h * chunks and threads == 256, (fmt, od, h, m)
+                else:
+                    tt = 32 if m <= 64 else (64 if m <= 128 else 128)
+                    assert grid == 4 * h * -(-m // tt) and threads == (256 if tt == 32 else 512), (fmt, od, h, m)
 
 
 @pytest.mark.parametrize("fmt,od", PAIRS)
@@ -106,7 +117,7 @@ def test_nope192(cuda_device, fmt, od):
 def test_small_integers_bit_exact(cuda_device, fmt, K):
     # Every partial sum is an integer of magnitude <= 2K: exact in FP32 in any
     # order, so the tensor-core result must equal the oracle bit for bit.
-    for H, M in ((16, 256), (11, 97), (8, 33)):
+    for H, M in ((16, 256), (11, 97), (8, 33), (8, 100)):
         d = inputs.small_integer_layer(300 + M, H, M, fmt, nope=K)
         for od, qs in (("bf16", None), ("e4m3", np.float32(0.25))):
             got = _rows(_run(_dev(d), M, H, fmt, od, qs, K=K), M, H, D * H, od)
@@ -187,15 +198,15 @@ def test_graph_chain_mixed_token_counts(cuda_device):
         check_output(_rows(outs[i], M, H, D * H, od), ref, acc, od, f"graph layer {i} {fmt}->{od} M{M}")
 
 
-@pytest.mark.parametrize("M", [64, 100])
-def test_bounded_wait_reports_timeout_and_frees_tmem(cuda_device, M):
+@pytest.mark.parametrize("H,M", [(8, 64), (8, 100), (16, 100)])
+def test_bounded_wait_reports_timeout_and_frees_tmem(cuda_device, H, M):
     # Every CTA's weight wait runs out (2 ms): the kernel records the timeout,
-    # writes nothing, and (M = 100, the tcgen05 kernel) releases its tensor
-    # memory; later runs (which allocate tensor memory again on the same SMs)
-    # still work.  M = 64 runs the CTA-tile kernel in two chunks.
+    # writes nothing, and (H = 16, M = 100: the tcgen05 kernel) releases its
+    # tensor memory; later runs (which allocate tensor memory again on the
+    # same SMs) still work.  H = 8 runs the CTA-tile kernel in two and four
+    # token chunks.
     st, _ = mq.mlaqp_device_status(reset=True)
     assert st == mq.MLAQP_OK
-    H = 8
     for fmt in ("bf16", "mxfp8"):
         d = inputs.make_layer(36, H, fmt, m_max=M)
         t = _dev(d)
