@@ -311,19 +311,22 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *                  16-byte aligned; rows >= M and the padding are not written;
  *                  may not overlap an input
  *   M              0 returns MLAQP_OK without launching; 1..256 supported
- *                  (up to 64: an mma.sync kernel over 32-token chunks, from
- *                  M = 9 (BF16) or 12 (MXFP8) launched in clusters of the 8
- *                  CTAs of a (head, chunk), which share x through one TMA
- *                  multicast per CTA where the strides form a tensor map;
- *                  above 64: a tcgen05 kernel launched in clusters of 4
- *                  CTAs, whose tensor memory is taken after the dependency
- *                  wait and freed before it returns)
+ *                  (an mma.sync kernel over 32-token chunks up to M = 64,
+ *                  and up to 128 while its 8*H*ceil(M/32) CTAs fit the
+ *                  device at two per SM; from M = 9 (BF16) or 12 (MXFP8)
+ *                  launched in clusters of the 8 CTAs of a (head, chunk),
+ *                  which share x through one TMA multicast per CTA where
+ *                  the strides form a tensor map.  Otherwise a tcgen05
+ *                  kernel launched in clusters of 4 CTAs, whose tensor
+ *                  memory is taken after the dependency wait and freed
+ *                  before it returns)
  *   H              8, 11 or 16
  *   pdl            1: programmatic dependent launch, as mlaqp_run_pdl (the
  *                  weights and scales must not be written by any kernel that
  *                  may still be running, see mlaqp_run_pdl); 2: the same,
- *                  and above M = 64 the next kernel may launch at this one's
- *                  entry, under the tensor-memory contract of
+ *                  and where the call runs the tcgen05 kernel the next kernel
+ *                  may launch at this one's entry, under the tensor-memory
+ *                  contract of
  *                  mlaqp_run_strided's pdl = 2; 0: ordinary launch; other
  *                  values return MLAQP_ERR_INVALID_ARG
  * Status codes as for mlaqp_run.

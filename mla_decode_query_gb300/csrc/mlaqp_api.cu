@@ -692,15 +692,23 @@ bool encode_v_x_map(CUtensorMap* map, const void* x, int64_t x_ts, int64_t x_hs,
   return r == CUDA_SUCCESS;
 }
 
-// Up to M = 64 the mma.sync kernel, in 32-token chunks (grid.z); above, the
-// tcgen05 cluster kernel.  Measured on GB300 (H = 16, BF16 W_UV, 128-layer
-// PDL chains, us per layer): the chunked kernel takes 3.0 / 3.0 / 5.8 / 9.4
-// at M = 33 / 64 / 128 / 256; the cluster kernel 3.23 at M = 65, 3.37 at
-// 128 and 4.80 at 256 (an earlier form of it, 3.41 / 3.55 at M = 33 / 64,
-// never beat the chunked kernel there).
+// The mma.sync kernels run in 32-token chunks (grid.z) up to M = 64, and up
+// to M = 128 while their 8*H*chunks CTAs fit the GPU at two per SM, as for
+// the query op; otherwise (from M = kVLargeMinM) the tcgen05 cluster
+// kernel.  Measured on GB300 (128-layer PDL chains, us per layer call,
+// cluster kernel / chunks): H = 8, M = 128: BF16 3.01 / 2.25, MXFP8 3.24 /
+// 2.76; H = 11, M = 96: BF16 3.03 / 2.32, MXFP8 3.25 / 2.79; H = 16 with
+// three or four chunks (384-512 CTAs): BF16 3.23-3.35 / 4.02-4.37.  Before
+// the x multicast the chunks took 3.0 / 5.8 / 9.4 at H = 16, M = 64 / 128
+// / 256.
 constexpr int kVLargeMinM = 65;
 
 int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }
+
+bool v_chunks_fit(int M, int H, int sm_count) {
+  if (M < kVLargeMinM) return true;
+  return M <= 128 && mlaqp::kVTilesPerHead * H * v_up_chunks(M) <= 2 * sm_count;
+}
 
 // From this M on the 8 CTAs of a (head, chunk) share x through a TMA
 // multicast.  Measured on GB300 (128-layer PDL chains, us per layer call,
@@ -776,7 +784,7 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lo
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  const bool large = M >= kVLargeMinM;
+  const bool large = !v_chunks_fit(M, H, g_dev[device].sm_count);
   const KernelInfo* k = nullptr;
   int smem_bytes = 0;
   int chunks = 0;

@@ -182,16 +182,15 @@ def test_graph_chain_with_query_projection(cuda_device, pdl):
         np.testing.assert_array_equal(qbits[..., 512:], dq["q_pe"])
 
 
-@pytest.mark.parametrize("M", [4, 20, 40, 100])
-def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device, M):
-    # M = 20 and 40 run the x-multicast kernel: every CTA gives up on its
-    # weight copy but still sends its x box and waits for the others'.
-    # M = 100 runs the tcgen05 cluster kernel: every CTA gives up on its
-    # weight copy but still passes both cluster barriers, and no cluster
-    # writes.
+@pytest.mark.parametrize("H,M", [(8, 4), (8, 20), (8, 40), (8, 100), (16, 100)])
+def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device, H, M):
+    # H = 8, M = 20 / 40 / 100 run the x-multicast kernel (1, 2 and 4 token
+    # chunks): every CTA gives up on its weight copy but still sends its x
+    # box and waits for the others'.  H = 16, M = 100 runs the tcgen05
+    # cluster kernel: every CTA gives up on its weight copy but still passes
+    # both cluster barriers, and no cluster writes.
     st, _ = mq.mlaqp_device_status(reset=True)
     assert st == mq.MLAQP_OK
-    H = 8
     for fmt in ("bf16", "mxfp8"):
         d = inputs.make_v_layer(56, H, fmt, m_max=M)
         t = _dev(d)
@@ -212,9 +211,10 @@ def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device, M):
 @pytest.mark.parametrize("fmt", ["bf16", "mxfp8"])
 @pytest.mark.parametrize("H", [8, 11, 16])
 def test_larger_token_counts(cuda_device, fmt, H):
-    # Above M = 32 the cluster kernel: token tiles of 32 / 64 / 128 and
-    # their edges, ragged tails (16-token MMA padding, chunks of 1 token),
-    # strided x and a pitched workspace.
+    # Above M = 32: the chunked kernels (H = 8 to M = 128, H = 11 to 96,
+    # H = 16 to 64) and the tcgen05 cluster kernel beyond, with token tiles
+    # of 64 / 128 and their edges, ragged tails (16-token MMA padding, chunks
+    # of 1 token), strided x and a pitched workspace.
     MM = 256
     d = inputs.make_v_layer(inputs.layer_seed(57, H), H, fmt, m_max=MM)
     _, acc = _oracle(d, fmt)
@@ -245,6 +245,11 @@ def test_larger_token_counts_bit_exact(cuda_device):
         for M in (64, 100, 256):
             got = _rows(_run(t, M, 16, fmt), M, 16, V * 16)
             np.testing.assert_array_equal(got, ref[:M], err_msg=f"{fmt} M{M}")
+        # H = 8: four 32-token chunks of the x-multicast kernel at M = 128
+        d8 = inputs.small_integer_v_layer(59, 8, 128, fmt)
+        ref8, _ = _oracle(d8, fmt)
+        got = _rows(_run(_dev(d8), 128, 8, fmt), 128, 8, V * 8)
+        np.testing.assert_array_equal(got, ref8, err_msg=f"{fmt} H8 M128")
 
 
 @pytest.mark.parametrize("M,qfmt,vfmt", [(20, "bf16", "mxfp8"), (40, "mxfp8", "bf16"), (5, "bf16", "bf16")])
