@@ -254,7 +254,7 @@ int nope_index(int K) {
 // Above M = 32 the CTA-tile kernel runs in 32-token chunks (grid.z; the
 // later chunks find the weight tile in L2) instead of the tcgen05 kernel:
 // always up to M = 64, and up to kCtaMaxM while all its CTAs fit on the GPU
-// at two per SM.  It needs no tensor memory, so it may trigger the next
+// at two, else three, per SM (cta_chunk_cap).  It needs no tensor memory, so it may trigger the next
 // launch at entry.  Measured on GB300 (128/256-layer PDL chains, pdl = 1, us
 // per layer call, tcgen05 / chunked): H = 16, BF16->BF16 2.43 / 2.08 at
 // M = 33 and 2.51 / 2.28 at 64; MXFP8->E4M3 3.22 / 2.43 and 3.34 / 2.52;
@@ -267,10 +267,19 @@ constexpr int kCtaAlwaysM = 64;
 
 int cta_chunks(int M) { return (M + mlaqp::kMaxM - 1) / mlaqp::kMaxM; }
 
-bool cta_chunks_fit(int M, int H, int sm_count) {
-  if (M <= kCtaAlwaysM) return true;
-  return M <= kCtaMaxM && mlaqp::kTilesPerHead * H * cta_chunks(M) <= 2 * sm_count;
+// CTAs per SM a chunked launch is capped at: 2 while its 8*H*chunks CTAs fit
+// at two per SM, else 3 while they fit at three (H = 16, M = 65..96: BF16
+// 2.42-2.52 us against 2.90 on tcgen05, MXFP8->E4M3 2.80-2.86 against
+// 3.24-3.28); 0 when they do not fit at all (then the tcgen05 kernel runs;
+// four chunks at H = 16 and cap 3 measured 4.0-4.6 us).
+int cta_chunk_cap(int M, int H, int sm_count) {
+  if (M <= kCtaAlwaysM) return 2;
+  if (M > kCtaMaxM) return 0;
+  const int ctas = mlaqp::kTilesPerHead * H * cta_chunks(M);
+  return ctas <= 2 * sm_count ? 2 : (ctas <= 3 * sm_count ? 3 : 0);
 }
+
+bool cta_chunks_fit(int M, int H, int sm_count) { return cta_chunk_cap(M, H, sm_count) != 0; }
 
 const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int nope_idx) {
   const int mt = ((M < mlaqp::kMaxM ? M : mlaqp::kMaxM) + 7) / 8;
@@ -600,7 +609,9 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
     k = lookup_large(a.weight_format, a.out_dtype, ki, large_tile_index(M), pdl == 2 ? 1 : 0);
     smem_bytes = large_smem(g_dev[device], k->smem_bytes, M);
   } else {
-    const LaunchPolicy pol = launch_policy(a.weight_format, a.out_dtype, M);
+    LaunchPolicy pol = launch_policy(a.weight_format, a.out_dtype, M);
+    if (M > MLAQP_MAX_M_DECODE && g_policy_trig.load(std::memory_order_relaxed) < 0)
+      pol.cta_cap = cta_chunk_cap(M, H, g_dev[device].sm_count);
     k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki);
     smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   }
@@ -705,10 +716,16 @@ constexpr int kVLargeMinM = 65;
 
 int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }
 
-bool v_chunks_fit(int M, int H, int sm_count) {
-  if (M < kVLargeMinM) return true;
-  return M <= 128 && mlaqp::kVTilesPerHead * H * v_up_chunks(M) <= 2 * sm_count;
+// CTAs per SM the chunked V launch needs (2, or 3 where 2 do not hold all
+// its CTAs), or 0 when they do not fit at three per SM.
+int v_chunk_cap(int M, int H, int sm_count) {
+  if (M < kVLargeMinM) return 2;
+  if (M > 128) return 0;
+  const int ctas = mlaqp::kVTilesPerHead * H * v_up_chunks(M);
+  return ctas <= 2 * sm_count ? 2 : (ctas <= 3 * sm_count ? 3 : 0);
 }
+
+bool v_chunks_fit(int M, int H, int sm_count) { return v_chunk_cap(M, H, sm_count) != 0; }
 
 // From this M on the 8 CTAs of a (head, chunk) share x through a TMA
 // multicast.  Measured on GB300 (128-layer PDL chains, us per layer call,
@@ -797,7 +814,8 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lo
   mlaqp::VUpParams params;
   bool mc = false;
   if (!large) {
-    const LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
+    LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
+    if (pol.cta_cap != 0 && M >= kVLargeMinM) pol.cta_cap = v_chunk_cap(M, H, g_dev[device].sm_count);
     const int trig = pol.trig == 0 ? 0 : 1;
     const int tt = 8 * (((M < mlaqp::kVChunk ? M : mlaqp::kVChunk) + 7) / 8);
     mc = M >= v_mc_min_m(a.weight_format) && encode_v_x_map(&params.xmap, a.x, a.x_ts, a.x_hs, M, H, tt);
