@@ -28,7 +28,7 @@
  *     prefill-sized steps that the pages leave to the staged BMM (vLLM PR
  *     #174, sections Safety scope and E2E topology matrix): the decode
  *     (mma.sync) kernel runs in 32-token chunks up to M = 64, and up to
- *     M = 128 while its 8*H*ceil(M/32) CTAs fit the device at two per SM;
+ *     M = 128 while its 8*H*ceil(M/32) CTAs fit the device at three per SM;
  *     beyond that a tcgen05 (TMEM-accumulator) kernel takes its place.
  *   - Status codes are the mlaqp_status values; on any non-OK status a
  *     message is available from mlaqp_last_error() on the same thread.
@@ -313,7 +313,7 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *   M              0 returns MLAQP_OK without launching; 1..256 supported
  *                  (an mma.sync kernel over 32-token chunks up to M = 64,
  *                  and up to 128 while its 8*H*ceil(M/32) CTAs fit the
- *                  device at two per SM; from M = 9 (BF16) or 12 (MXFP8)
+ *                  device at three per SM; from M = 9 (BF16) or 12 (MXFP8)
  *                  launched in clusters of the 8 CTAs of a (head, chunk),
  *                  which share x through one TMA multicast per CTA where
  *                  the strides form a tensor map.  Otherwise a tcgen05
