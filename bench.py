@@ -237,7 +237,8 @@ class VLayerSet:
     def kernel_name(self, M):
         import torch
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        if M > 64 and not (M <= 128 and 8 * self.H * -(-M // 32) <= 3 * sms):  # the library's fit rule
+        ctas = 8 * self.H * -(-M // 32)
+        if M > 64 and 5 * ctas > 13 * sms:  # the library's fit rule (at most 2.6 CTAs per SM)
             return "mlaqp_v_up_large_kernel"
         # the library's switch to the x-multicast kernel (BF16 from M = 9, MXFP8 from M = 12)
         return "mlaqp_v_up_mc_kernel" if M >= V_MC_MIN_M[self.weight_format] else "mlaqp_v_up_kernel"

@@ -262,7 +262,7 @@ int nope_index(int K) {
 // trigger 2.68 / 2.74).  H = 8 (four chunks, 256 CTAs), M = 128: BF16->BF16
 // 2.83 / 2.09, MXFP8->E4M3 3.27 / 2.39.  H = 16 with three or four chunks
 // (384-512 CTAs, more than fit): 3.6-4.7 against 2.8-3.5.
-constexpr int kCtaMaxM = 128;
+constexpr int kCtaMaxM = MLAQP_MAX_M;
 constexpr int kCtaAlwaysM = 64;
 
 int cta_chunks(int M) { return (M + mlaqp::kMaxM - 1) / mlaqp::kMaxM; }
@@ -271,7 +271,10 @@ int cta_chunks(int M) { return (M + mlaqp::kMaxM - 1) / mlaqp::kMaxM; }
 // at two per SM, else 3 while they fit at three (H = 16, M = 65..96: BF16
 // 2.42-2.52 us against 2.90 on tcgen05, MXFP8->E4M3 2.80-2.86 against
 // 3.24-3.28); 0 when they do not fit at all (then the tcgen05 kernel runs;
-// four chunks at H = 16 and cap 3 measured 4.0-4.6 us).
+// four chunks at H = 16 and cap 3 measured 4.0-4.6 us).  Above M = 128
+// only H = 8 (to 224 tokens, up to 448 CTAs) and H = 11 (to 160) fit:
+// H = 8, M = 192: BF16 3.64 / 2.42, MXFP8->E4M3 3.60 / 2.78; H = 11,
+// M = 160: 3.74 / 2.65 and 3.62 / 3.02 (tcgen05 / chunks).
 int cta_chunk_cap(int M, int H, int sm_count) {
   if (M <= kCtaAlwaysM) return 2;
   if (M > kCtaMaxM) return 0;
@@ -599,7 +602,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
     return fail(MLAQP_ERR_UNSUPPORTED, "the CUDA-core arm covers M <= 8 at nope_dim 128");
   if (arm == Arm::kWarpMma && M > MLAQP_MAX_M_DECODE)
     return fail(MLAQP_ERR_UNSUPPORTED, "the warp-tile arm covers M <= 32");
-  if (arm == Arm::kCtaMma && M > kCtaMaxM) return fail(MLAQP_ERR_UNSUPPORTED, "the CTA-tile arm covers M <= 128");
+  if (arm == Arm::kCtaMma && M > kCtaMaxM) return fail(MLAQP_ERR_UNSUPPORTED, "the CTA-tile arm covers M <= 256");
   if (arm == Arm::kWarpMma || arm == Arm::kWarpFma) return launch_warp(a, stream, pdl, wait_limit_ns, extra_tx, arm, device);
 
   const bool large = arm == Arm::kTcgen05;
@@ -718,12 +721,15 @@ constexpr int kVLargeMinM = 65;
 int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }
 
 // CTAs per SM the chunked V launch needs (2, or 3 where 2 do not hold all
-// its CTAs), or 0 when they do not fit at three per SM.
+// its CTAs), or 0 when it should not run.  The 8-CTA clusters place less
+// freely than the query's CTAs: at 384 CTAs (H = 8, M = 192; H = 16, M = 96)
+// the chunks still win (BF16 4.08 / 2.75 and 3.29 / 2.80 us, cluster kernel
+// / chunks), at 440-448 (H = 11, M = 160; H = 8, M = 224) they lose (4.17 /
+// 4.35, 4.11 / 4.42), so the three-per-SM tier stops at 2.6 CTAs per SM.
 int v_chunk_cap(int M, int H, int sm_count) {
   if (M < kVLargeMinM) return 2;
-  if (M > 128) return 0;
   const int ctas = mlaqp::kVTilesPerHead * H * v_up_chunks(M);
-  return ctas <= 2 * sm_count ? 2 : (ctas <= 3 * sm_count ? 3 : 0);
+  return ctas <= 2 * sm_count ? 2 : (5 * ctas <= 13 * sm_count ? 3 : 0);
 }
 
 bool v_chunks_fit(int M, int H, int sm_count) { return v_chunk_cap(M, H, sm_count) != 0; }

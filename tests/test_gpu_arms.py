@@ -114,7 +114,7 @@ def test_arms_reject_calls_they_do_not_cover(cuda_device):
     d = inputs.make_layer(1, 8, "bf16", m_max=136, nope=192)
     t = _dev(d)
     out = torch.zeros((136 * D * 8,), dtype=torch.int16, device="cuda")
-    for M, K, arm in ((9, 128, "warp_fma"), (4, 192, "warp_fma"), (33, 192, "warp_mma"), (129, 192, "cta_mma")):
+    for M, K, arm in ((9, 128, "warp_fma"), (4, 192, "warp_fma"), (33, 192, "warp_mma"), (257, 192, "cta_mma")):
         st = mq.mlaqp_debug_run_arm(t["q_nope"], 8 * K, K, t["q_pe"], 8 * 64, 64, t["weight"], None, out, D * 8,
                                     None, M, 8, K, "bf16", "bf16", arm=arm)
         assert st == mq.MLAQP_ERR_UNSUPPORTED, (M, K, arm)
