@@ -27,9 +27,10 @@
  *     pages; 33..256 extends it to the multi-token-prediction and
  *     prefill-sized steps that the pages leave to the staged BMM (vLLM PR
  *     #174, sections Safety scope and E2E topology matrix): the decode
- *     (mma.sync) kernel runs in 32-token chunks up to M = 64, and up to
- *     M = 128 while its 8*H*ceil(M/32) CTAs fit the device at three per SM;
- *     beyond that a tcgen05 (TMEM-accumulator) kernel takes its place.
+ *     (mma.sync) kernel runs in 32-token chunks up to M = 64, and beyond
+ *     while its 8*H*ceil(M/32) CTAs fit the device at three per SM (H = 8 to
+ *     M = 224, H = 11 to 160, H = 16 to 96 on 152 SMs); otherwise a tcgen05
+ *     (TMEM-accumulator) kernel takes its place.
  *   - Status codes are the mlaqp_status values; on any non-OK status a
  *     message is available from mlaqp_last_error() on the same thread.
  *
@@ -248,7 +249,7 @@ int mlaqp_debug_run_bounded_wait(const void* q_nope, const void* q_pe, const voi
  *                       cores with a warp-shuffle reduction (M <= 8,
  *                       nope_dim 128)
  *   MLAQP_ARM_CTA_MMA   the CTA-tile mma.sync kernel (64 latent columns per
- *                       CTA, q_nope staged in shared memory; M <= 128, in
+ *                       CTA, q_nope staged in shared memory; any M, in
  *                       32-token chunks above 32)
  *   MLAQP_ARM_TCGEN05   the tcgen05 kernel (TMEM accumulator; any M)
  * A form that does not cover the call returns MLAQP_ERR_UNSUPPORTED; every
@@ -312,8 +313,9 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *                  may not overlap an input
  *   M              0 returns MLAQP_OK without launching; 1..256 supported
  *                  (an mma.sync kernel over 32-token chunks up to M = 64,
- *                  and up to 128 while its 8*H*ceil(M/32) CTAs fit the
- *                  device at three per SM; from M = 9 (BF16) or 12 (MXFP8)
+ *                  and beyond while its 8*H*ceil(M/32) CTAs stay within 2.6
+ *                  per SM (H = 8 to M = 192, H = 11 to 128, H = 16 to 96 on
+ *                  152 SMs); from M = 9 (BF16) or 12 (MXFP8)
  *                  launched in clusters of the 8 CTAs of a (head, chunk),
  *                  which share x through one TMA multicast per CTA where
  *                  the strides form a tensor map.  Otherwise a tcgen05
