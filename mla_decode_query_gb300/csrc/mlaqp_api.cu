@@ -706,11 +706,11 @@ bool encode_v_x_map(CUtensorMap* map, const void* x, int64_t x_ts, int64_t x_hs,
   return r == CUDA_SUCCESS;
 }
 
-// The mma.sync kernels run in 32-token chunks (grid.z) up to M = 64, and up
-// to M = 128 while their 8*H*chunks CTAs fit the GPU at two, else three,
-// per SM (BF16 capped accordingly, MXFP8 uncapped), as for the query op;
-// otherwise (from M = kVLargeMinM) the tcgen05 cluster kernel (H = 16,
-// M = 96: BF16 3.29 / 2.80 at cap 3, MXFP8 3.42 / 3.20).  Measured on GB300 (128-layer PDL chains, us per layer call,
+// The mma.sync kernels run in 32-token chunks (grid.z) up to M = 64, and
+// beyond while their 8*H*chunks CTAs fit the GPU (v_chunk_cap; BF16 capped
+// accordingly, MXFP8 uncapped); otherwise (from M = kVLargeMinM) the
+// tcgen05 cluster kernel (H = 16, M = 96: BF16 3.29 / 2.80 at cap 3, MXFP8
+// 3.42 / 3.20).  Measured on GB300 (128-layer PDL chains, us per layer call,
 // cluster kernel / chunks): H = 8, M = 128: BF16 3.01 / 2.25, MXFP8 3.24 /
 // 2.76; H = 11, M = 96: BF16 3.03 / 2.32, MXFP8 3.25 / 2.79; H = 16 with
 // three or four chunks (384-512 CTAs): BF16 3.23-3.35 / 4.02-4.37.  Before
