@@ -713,7 +713,7 @@ bool encode_v_x_map(CUtensorMap* map, const void* x, int64_t x_ts, int64_t x_hs,
 // 3.42 / 3.20).  Measured on GB300 (128-layer PDL chains, us per layer call,
 // cluster kernel / chunks): H = 8, M = 128: BF16 3.01 / 2.25, MXFP8 3.24 /
 // 2.76; H = 11, M = 96: BF16 3.03 / 2.32, MXFP8 3.25 / 2.79; H = 16 with
-// three or four chunks (384-512 CTAs): BF16 3.23-3.35 / 4.02-4.37.  Before
+// three or four chunks at cap 2 (384-512 CTAs): BF16 3.23-3.35 / 4.02-4.37.  Before
 // the x multicast the chunks took 3.0 / 5.8 / 9.4 at H = 16, M = 64 / 128
 // / 256.
 constexpr int kVLargeMinM = 65;
