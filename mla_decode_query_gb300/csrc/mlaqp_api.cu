@@ -285,11 +285,11 @@ int cta_chunk_cap(int M, int H, int sm_count) {
 bool cta_chunks_fit(int M, int H, int sm_count) { return cta_chunk_cap(M, H, sm_count) != 0; }
 
 const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int nope_idx) {
-  const int mt = ((M < mlaqp::kMaxM ? M : mlaqp::kMaxM) + 7) / 8;
-  if (mt < 1 || mt > 4) return nullptr;
+  if (M < 1) return nullptr;
+  const int form = M > mlaqp::kMaxM ? mlaqp::kChunkedForm : (M + 7) / 8 - 1;
   const mlaqp::KernelTable& table =
       weight_format == MLAQP_WEIGHT_BF16 ? mlaqp::kernels_bf16_weights() : mlaqp::kernels_mxfp8_weights();
-  return &table[nope_idx][out_dtype][mt - 1][trig];
+  return &table[nope_idx][out_dtype][form][trig];
 }
 
 // Token tile (tokens per CTA) of a large-M call, as an index into
@@ -381,7 +381,7 @@ int setup_kernels(const DeviceInfo& d) {
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
       for (int od = 0; od < 2; ++od)
-        for (int mt = 1; mt <= 4; ++mt)
+        for (int mt = 1; mt <= 5; ++mt)  // 5: the chunked form (any M > 32)
           for (int trig = 0; trig < mlaqp::kTrigVariants; ++trig) {
             const KernelInfo* k = lookup(wf, od, 8 * mt, trig, ki);
             const cudaError_t e = cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -936,6 +936,12 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
         cudaFuncAttributes attr;
         e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti, 0)->fn);
         if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti, 1)->fn);
+        if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
+      }
+    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)  // the chunked CTA-tile form
+      for (int trig = 0; trig < mlaqp::kTrigVariants && status == MLAQP_OK; ++trig) {
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, lookup(weight_format, out_dtype, mlaqp::kMaxM + 1, trig, ki)->fn);
         if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
       }
     if (status == MLAQP_OK) g_prewarmed[dev].fetch_or(large_bit, std::memory_order_acq_rel);

@@ -13,13 +13,16 @@ struct KernelInfo {
   int smem_bytes;      // dynamic shared memory per CTA
 };
 
-// Table [nope][out_dtype][mt-1][trig]: nope 0 = K 128, 1 = K 192;
-// mt = ceil(M/8) in 1..4; trig = where the CTA triggers the next kernel's
+// Table [nope][out_dtype][form][trig]: nope 0 = K 128, 1 = K 192; form
+// mt-1 for mt = ceil(M/8) in 1..4 (M <= 32, one launch covers all tokens),
+// and form 4 for M > 32 (four token tiles per 32-token chunk, grid.z
+// chunks); trig = where the CTA triggers the next kernel's
 // launch (0: at entry, 1: after the dependency wait, 2: once its weight
 // tile is ready).
 constexpr int kTrigVariants = 3;
 constexpr int kNopeDims[2] = {128, 192};
-using KernelTable = KernelInfo[2][2][4][kTrigVariants];
+constexpr int kChunkedForm = 4;
+using KernelTable = KernelInfo[2][2][5][kTrigVariants];
 
 const KernelTable& kernels_bf16_weights();
 const KernelTable& kernels_mxfp8_weights();

@@ -6,21 +6,22 @@ namespace mlaqp {
 namespace {
 constexpr int kWF = kWeightMXFP8;
 
-template <int K, int OD, int MT, int TRIG>
+template <int K, int OD, int MT, int TRIG, int CH>
 KernelInfo entry() {
-  return KernelInfo{reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT, TRIG, K>),
-                    kThreads * token_groups(MT), kTilesPerHead, Smem<K>::Bytes};
+  return KernelInfo{
+      reinterpret_cast<const void*>(&mlaqp_fused_query_kernel<kWF, OD, MT, TRIG, K, token_groups(MT), CH>),
+      kThreads * token_groups(MT), kTilesPerHead, Smem<K>::Bytes};
 }
 
-template <int K, int OD, int MT>
+template <int K, int OD, int MT, int CH = 0>
 void fill(KernelInfo (&row)[kTrigVariants]) {
-  row[0] = entry<K, OD, MT, 0>();
-  row[1] = entry<K, OD, MT, 1>();
-  row[2] = entry<K, OD, MT, 2>();
+  row[0] = entry<K, OD, MT, 0, CH>();
+  row[1] = entry<K, OD, MT, 1, CH>();
+  row[2] = entry<K, OD, MT, 2, CH>();
 }
 
 template <int K>
-void fill_nope(KernelInfo (&t)[2][4][kTrigVariants]) {
+void fill_nope(KernelInfo (&t)[2][5][kTrigVariants]) {
   fill<K, kOutBF16, 1>(t[0][0]);
   fill<K, kOutBF16, 2>(t[0][1]);
   fill<K, kOutBF16, 3>(t[0][2]);
@@ -29,6 +30,8 @@ void fill_nope(KernelInfo (&t)[2][4][kTrigVariants]) {
   fill<K, kOutE4M3, 2>(t[1][1]);
   fill<K, kOutE4M3, 3>(t[1][2]);
   fill<K, kOutE4M3, 4>(t[1][3]);
+  fill<K, kOutBF16, 4, 1>(t[0][kChunkedForm]);  // M > 32: 32-token chunks
+  fill<K, kOutE4M3, 4, 1>(t[1][kChunkedForm]);
 }
 
 struct Table {
