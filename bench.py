@@ -145,7 +145,9 @@ class LayerSet:
         if self.arm == "auto":
             import mla_decode_query_gb300 as mq
             st, grid, _ = mq.mlaqp_launch_shape(M, self.H, self.weight_format, self.out_dtype)
-            cta = st == 0 and grid == 8 * self.H * -(-M // 32)  # the CTA-tile kernel, one CTA per 32-token chunk
+            # the CTA-tile kernel launches 8*H CTAs per token chunk; the warp-tile
+            # kernel's SM-count grid (152) is no multiple of 8*H for H = 8, 11, 16
+            cta = st == 0 and grid % (8 * self.H) == 0
             if M > 32:
                 return "mlaqp_fused_query_kernel" if cta else "mlaqp_fused_query_large_kernel"
             return "mlaqp_fused_query_kernel" if cta else "mlaqp_query_warp_kernel"

@@ -284,9 +284,33 @@ int cta_chunk_cap(int M, int H, int sm_count) {
 
 bool cta_chunks_fit(int M, int H, int sm_count) { return cta_chunk_cap(M, H, sm_count) != 0; }
 
-const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int nope_idx) {
+// Tokens per chunk of a CTA-tile launch: 32 above M = 32; for 9 <= M <= 32
+// with nope dim 128, 8 (M <= 16) or 16 (MXFP8 weights, M = 17..32) where
+// the two chunks' 16*H CTAs fit one per SM (H = 8 on 152 SMs); else 0, one
+// launch over all tokens.  Measured on GB300 (128/256-layer PDL chains, us
+// per layer call, H = 8, current choice / two chunks): M = 16: BF16->BF16
+// 1.47 / 1.35, MXFP8->E4M3 1.53 / 1.38, BF16->E4M3 1.51 / 1.37; M = 32:
+// MXFP8->E4M3 1.67 / 1.53, MXFP8->BF16 1.60 / 1.51.  With BF16 weights at
+// M = 17..32 the chunks tie or lose (1.60-1.63 against 1.55-1.61), and at
+// H = 16 (256 CTAs, two per SM) they lose at every M (0.2-0.5 us).
+int cta_chunk_len(int weight_format, int M, int H, int K, int sm_count) {
+  if (M > mlaqp::kMaxM) return mlaqp::kMaxM;
+  if (M <= 8 || K != MLAQP_NOPE_DIM || 2 * mlaqp::kTilesPerHead * H > sm_count) return 0;
+  if (M <= 16) return 8;
+  return weight_format == MLAQP_WEIGHT_MXFP8 ? 16 : 0;
+}
+
+int cta_form(int M, int chunk) {
+  if (chunk == 32) return mlaqp::kChunkedForm;
+  if (chunk == 16) return mlaqp::kChunked16Form;
+  if (chunk == 8) return mlaqp::kChunked8Form;
+  return (M + 7) / 8 - 1;
+}
+
+// chunk < 0: the chunk length of a launch that splits only above M = 32.
+const KernelInfo* lookup(int weight_format, int out_dtype, int M, int trig, int nope_idx, int chunk = -1) {
   if (M < 1) return nullptr;
-  const int form = M > mlaqp::kMaxM ? mlaqp::kChunkedForm : (M + 7) / 8 - 1;
+  const int form = cta_form(M, chunk < 0 ? (M > mlaqp::kMaxM ? mlaqp::kMaxM : 0) : chunk);
   const mlaqp::KernelTable& table =
       weight_format == MLAQP_WEIGHT_BF16 ? mlaqp::kernels_bf16_weights() : mlaqp::kernels_mxfp8_weights();
   return &table[nope_idx][out_dtype][form][trig];
@@ -381,9 +405,10 @@ int setup_kernels(const DeviceInfo& d) {
   for (int ki = 0; ki < 2; ++ki)
     for (int wf = 0; wf < 2; ++wf)
       for (int od = 0; od < 2; ++od)
-        for (int mt = 1; mt <= 5; ++mt)  // 5: the chunked form (any M > 32)
+        for (int form = 0; form <= mlaqp::kChunked16Form; ++form)
           for (int trig = 0; trig < mlaqp::kTrigVariants; ++trig) {
-            const KernelInfo* k = lookup(wf, od, 8 * mt, trig, ki);
+            const mlaqp::KernelTable& table = wf == 0 ? mlaqp::kernels_bf16_weights() : mlaqp::kernels_mxfp8_weights();
+            const KernelInfo* k = &table[ki][od][form][trig];
             const cudaError_t e = cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute", e);
           }
@@ -454,9 +479,10 @@ int warp_crossover(int weight_format, int out_dtype, int H) {
   return out_dtype == MLAQP_OUT_BF16 ? 13 : 16;
 }
 
-// sm_count is read only above M = kCtaAlwaysM.
+// sm_count: the device's SM count (the chunk rules depend on it).
 Arm auto_arm(int weight_format, int out_dtype, int M, int H, int K, int sm_count) {
   if (M > MLAQP_MAX_M_DECODE) return cta_chunks_fit(M, H, sm_count) ? Arm::kCtaMma : Arm::kTcgen05;
+  if (cta_chunk_len(weight_format, M, H, K, sm_count) != 0) return Arm::kCtaMma;
   if (M < warp_crossover(weight_format, out_dtype, H)) return Arm::kCtaMma;
   if (K != MLAQP_NOPE_DIM && M > 24 && !(weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3))
     return Arm::kCtaMma;
@@ -608,6 +634,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
   const bool large = arm == Arm::kTcgen05;
   const KernelInfo* k = nullptr;
   int smem_bytes = 0;
+  int chunk = 0;  // tokens per chunk of a CTA-tile launch (0: one launch over all M)
   if (large) {
     k = lookup_large(a.weight_format, a.out_dtype, ki, large_tile_index(M), pdl == 2 ? 1 : 0);
     smem_bytes = large_smem(g_dev[device], k->smem_bytes, M);
@@ -615,7 +642,8 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
     LaunchPolicy pol = launch_policy(a.weight_format, a.out_dtype, M);
     if (M > MLAQP_MAX_M_DECODE && g_policy_trig.load(std::memory_order_relaxed) < 0)
       pol.cta_cap = cta_chunk_cap(M, H, g_dev[device].sm_count);
-    k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki);
+    chunk = cta_chunk_len(a.weight_format, M, H, K, g_dev[device].sm_count);
+    k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki, chunk);
     smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   }
   RunParams params;
@@ -638,7 +666,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H),
-                     static_cast<unsigned>(large ? large_chunks(M) : cta_chunks(M)));
+                     static_cast<unsigned>(large ? large_chunks(M) : (chunk ? (M + chunk - 1) / chunk : 1)));
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -916,6 +944,8 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
         const KernelInfo* k = lookup(weight_format, out_dtype, 8 * mt, trig, ki);
         cudaFuncAttributes attr;
         e = cudaFuncGetAttributes(&attr, k->fn);  // forces the kernel image to load
+        if (e == cudaSuccess && mt >= 2)           // and its 8- / 16-token chunked form
+          e = cudaFuncGetAttributes(&attr, lookup(weight_format, out_dtype, 8 * mt, trig, ki, mt == 2 ? 8 : 16)->fn);
         if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
       }
       for (int trig = 0; trig < 2 && status == MLAQP_OK; ++trig) {
@@ -938,7 +968,7 @@ int mlaqp_prewarm(int num_heads, int max_m, int weight_format, int out_dtype, in
         if (e == cudaSuccess) e = cudaFuncGetAttributes(&attr, lookup_large(weight_format, out_dtype, ki, ti, 1)->fn);
         if (e != cudaSuccess) status = fail_cuda("cudaFuncGetAttributes", e);
       }
-    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)  // the chunked CTA-tile form
+    for (int ki = 0; ki < 2 && status == MLAQP_OK; ++ki)  // the 32-token chunked CTA-tile form
       for (int trig = 0; trig < mlaqp::kTrigVariants && status == MLAQP_OK; ++trig) {
         cudaFuncAttributes attr;
         e = cudaFuncGetAttributes(&attr, lookup(weight_format, out_dtype, mlaqp::kMaxM + 1, trig, ki)->fn);
@@ -979,13 +1009,15 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
   if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_UNSUPPORTED, "unknown weight_format or out_dtype");
   if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
   int sm_count = 0;
-  if (M > kCtaAlwaysM) {  // the choice depends on the device's SM count
+  if (M > 8) {  // the choice depends on the device's SM count, except at 33..64
     int dev = 0;
     int st = resolve_device(-1, &dev);
-    if (st != MLAQP_OK) return st;
-    st = check_device(dev);
-    if (st != MLAQP_OK) return st;
-    sm_count = g_dev[dev].sm_count;
+    if (st == MLAQP_OK) st = check_device(dev);
+    if (st == MLAQP_OK) {
+      sm_count = g_dev[dev].sm_count;
+    } else if (M <= MLAQP_MAX_M_DECODE || M > kCtaAlwaysM) {
+      return st;
+    }
   }
   const Arm arm = auto_arm(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM, sm_count);
   if (arm == Arm::kTcgen05) {
@@ -995,8 +1027,10 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
     return MLAQP_OK;
   }
   if (arm == Arm::kCtaMma) {
-    const KernelInfo* k = lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0);
-    if (grid_ctas) *grid_ctas = k->tiles_per_head * H * cta_chunks(M);
+    const int chunk = cta_chunk_len(weight_format, M, H, MLAQP_NOPE_DIM, sm_count);
+    const KernelInfo* k =
+        lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0, chunk);
+    if (grid_ctas) *grid_ctas = k->tiles_per_head * H * (chunk ? (M + chunk - 1) / chunk : 1);
     if (threads_per_cta) *threads_per_cta = k->threads;
     return MLAQP_OK;
   }

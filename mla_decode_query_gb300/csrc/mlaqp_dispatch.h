@@ -14,15 +14,17 @@ struct KernelInfo {
 };
 
 // Table [nope][out_dtype][form][trig]: nope 0 = K 128, 1 = K 192; form
-// mt-1 for mt = ceil(M/8) in 1..4 (M <= 32, one launch covers all tokens),
-// and form 4 for M > 32 (four token tiles per 32-token chunk, grid.z
-// chunks); trig = where the CTA triggers the next kernel's
+// mt-1 for mt = ceil(M/8) in 1..4 (one launch covers all tokens), and the
+// chunked forms (grid.z chunks of 8*mt tokens): 4 = 32-token chunks (M > 32),
+// 5 = 8-token chunks, 6 = 16-token chunks; trig = where the CTA triggers the next kernel's
 // launch (0: at entry, 1: after the dependency wait, 2: once its weight
 // tile is ready).
 constexpr int kTrigVariants = 3;
 constexpr int kNopeDims[2] = {128, 192};
 constexpr int kChunkedForm = 4;
-using KernelTable = KernelInfo[2][2][5][kTrigVariants];
+constexpr int kChunked8Form = 5;
+constexpr int kChunked16Form = 6;
+using KernelTable = KernelInfo[2][2][7][kTrigVariants];
 
 const KernelTable& kernels_bf16_weights();
 const KernelTable& kernels_mxfp8_weights();

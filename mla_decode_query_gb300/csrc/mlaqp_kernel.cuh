@@ -493,12 +493,12 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   const int lane = tid & 31;
   const int wcol = warp & (kWarps - 1);  // 16-column MMA tile of this warp
   const int wtok = warp / kWarps;        // token group of this warp
-  // CH = 1 (M > 32): this CTA's tokens are [m0, m0 + M) of a 32-token chunk
-  // (the grid has ceil(M / 32) of them); CH = 0: all tokens, with no offset
-  // arithmetic on the path (measured 0.02-0.13 us per layer call slower
-  // when M <= 32 launches carried it).
-  const int m0 = CH ? static_cast<int>(blockIdx.z) * kMaxM : 0;
-  const int M = CH ? min(kMaxM, p.M - m0) : p.M;
+  // CH = 1: this CTA's tokens are [m0, m0 + M) of an (8*MT)-token chunk
+  // (the grid has ceil(M / (8*MT)) of them); CH = 0: all tokens, with no
+  // offset arithmetic on the path (measured 0.02-0.13 us per layer call
+  // slower when unchunked launches carried it).
+  const int m0 = CH ? static_cast<int>(blockIdx.z) * 8 * MT : 0;
+  const int M = CH ? min(8 * MT, p.M - m0) : p.M;
   const int n_cta = tile * kNTile;
   // (Each use below reads the parameter itself when CH = 0, as before.)
   const uint16_t* const q_nope_c = p.q_nope + m0 * p.q_nope_ts;

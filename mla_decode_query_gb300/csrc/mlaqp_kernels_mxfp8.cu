@@ -21,7 +21,7 @@ void fill(KernelInfo (&row)[kTrigVariants]) {
 }
 
 template <int K>
-void fill_nope(KernelInfo (&t)[2][5][kTrigVariants]) {
+void fill_nope(KernelInfo (&t)[2][7][kTrigVariants]) {
   fill<K, kOutBF16, 1>(t[0][0]);
   fill<K, kOutBF16, 2>(t[0][1]);
   fill<K, kOutBF16, 3>(t[0][2]);
@@ -32,6 +32,10 @@ void fill_nope(KernelInfo (&t)[2][5][kTrigVariants]) {
   fill<K, kOutE4M3, 4>(t[1][3]);
   fill<K, kOutBF16, 4, 1>(t[0][kChunkedForm]);  // M > 32: 32-token chunks
   fill<K, kOutE4M3, 4, 1>(t[1][kChunkedForm]);
+  fill<K, kOutBF16, 1, 1>(t[0][kChunked8Form]);  // M = 9..32 on small H: 8- and 16-token chunks
+  fill<K, kOutE4M3, 1, 1>(t[1][kChunked8Form]);
+  fill<K, kOutBF16, 2, 1>(t[0][kChunked16Form]);
+  fill<K, kOutE4M3, 2, 1>(t[1][kChunked16Form]);
 }
 
 struct Table {

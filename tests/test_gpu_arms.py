@@ -136,7 +136,11 @@ def test_launch_shape_follows_the_policy(cuda_device):
             for m in (1, 8, 9, 12, 13, 14, 15, 16, 17, 32):
                 st, grid, threads = mq.mlaqp_launch_shape(m, h, fmt, od)
                 assert st == mq.MLAQP_OK
-                if m >= _crossover(fmt, od, h):
+                # two chunks of the CTA-tile kernel (8 tokens up to M = 16, 16 tokens
+                # for MXFP8 weights above) where their 16*H CTAs fit one per SM
+                if m > 8 and 16 * h <= sms and (m <= 16 or fmt == "mxfp8"):
+                    assert grid == 16 * h and threads == (128 if m <= 16 else 256), (fmt, od, h, m)
+                elif m >= _crossover(fmt, od, h):
                     assert grid == g and threads == 32 * tpc * (1 if m <= 8 else 2), (fmt, od, h, m)
                 else:
                     assert grid == 8 * h and threads == (128 if m <= 8 else 256), (fmt, od, h, m)
