@@ -748,6 +748,18 @@ constexpr int kVLargeMinM = 65;
 
 int v_up_chunks(int M) { return (M + mlaqp::kVChunk - 1) / mlaqp::kVChunk; }
 
+// Tokens per chunk of a V launch at 9 <= M <= 32 where two chunks' 16*H
+// CTAs fit one per SM (H = 8 on 152 SMs): 8 up to M = 16, 16 above for
+// MXFP8 weights; 0 when one launch covers all tokens.  Measured on GB300
+// (128/256-layer PDL chains, us per layer call, H = 8, one launch / two
+// chunks): M = 16: BF16 1.72 / 1.48, MXFP8 1.73 / 1.53; M = 32: MXFP8 2.17
+// / 1.69; BF16 at M = 17..32 1.82 / 1.85-1.87 (kept in one launch).
+int v_small_chunk(int weight_format, int M, int H, int sm_count) {
+  if (M <= 8 || M > mlaqp::kVChunk || 2 * mlaqp::kVTilesPerHead * H > sm_count) return 0;
+  if (M <= 16) return 8;
+  return weight_format == MLAQP_WEIGHT_MXFP8 ? 16 : 0;
+}
+
 // CTAs per SM the chunked V launch needs (2, or 3 where 2 do not hold all
 // its CTAs), or 0 when it should not run.  The 8-CTA clusters place less
 // freely than the query's CTAs: at 384 CTAs (H = 8, M = 192; H = 16, M = 96)
@@ -852,10 +864,14 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lo
     LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
     if (pol.cta_cap != 0 && M >= kVLargeMinM) pol.cta_cap = v_chunk_cap(M, H, g_dev[device].sm_count);
     const int trig = pol.trig == 0 ? 0 : 1;
-    const int tt = 8 * (((M < mlaqp::kVChunk ? M : mlaqp::kVChunk) + 7) / 8);
-    mc = M >= v_mc_min_m(a.weight_format) && encode_v_x_map(&params.xmap, a.x, a.x_ts, a.x_hs, M, H, tt);
-    k = mc ? lookup_v_up_mc(a.weight_format, M, trig) : lookup_v_up(a.weight_format, M, trig);
-    chunks = v_up_chunks(M);
+    const int vch = v_small_chunk(a.weight_format, M, H, g_dev[device].sm_count);
+    const int cm = vch ? vch : (M < mlaqp::kVChunk ? M : mlaqp::kVChunk);  // tokens per CTA chunk
+    const int tt = 8 * ((cm + 7) / 8);
+    // 8-token chunks read x with plain loads (x is 8 KB per CTA there)
+    mc = vch != 8 && M >= v_mc_min_m(a.weight_format) &&
+         encode_v_x_map(&params.xmap, a.x, a.x_ts, a.x_hs, M, H, tt);
+    k = mc ? lookup_v_up_mc(a.weight_format, cm, trig) : lookup_v_up(a.weight_format, cm, trig);
+    chunks = vch ? (M + vch - 1) / vch : v_up_chunks(M);
     smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
   }
   st = encode_v_weight_map(&params.wmap, a.weight, H, mx, large);

@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int m0 = blockIdx.z * kVChunk;   // this CTA's tokens: [m0, m0 + M)
-  const int M = min(kVChunk, p.M - m0);   // >= 1: the grid has ceil(M/32) chunks
+  const int m0 = blockIdx.z * 8 * MT;    // this CTA's tokens: [m0, m0 + M) of an (8*MT)-token chunk
+  const int M = min(8 * MT, p.M - m0);    // >= 1: the grid has ceil(M/(8*MT)) chunks
   const int d_cta = tile * kVNTile;
   const uint16_t* xh = p.x + m0 * p.x_ts + h * p.x_hs;
   uint16_t* const outc = p.out + m0 * p.out_row_stride;

@@ -87,8 +87,8 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_mc_kernel(const __grid_c
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int m0 = blockIdx.z * kVChunk;
-  const int M = min(kVChunk, p.M - m0);  // >= 1
+  const int m0 = blockIdx.z * TT;       // this CTA's tokens: [m0, m0 + M) of a TT-token chunk
+  const int M = min(TT, p.M - m0);      // >= 1
   const int d_cta = tile * kVNTile;
   uint16_t* const outc = p.out + m0 * p.out_row_stride;
 
