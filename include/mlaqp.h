@@ -315,7 +315,8 @@ int mlaqp_debug_launch_null(int ctas, int threads, int pdl, mlaqp_stream_t strea
  *                  (an mma.sync kernel over 32-token chunks up to M = 64,
  *                  and beyond while its 8*H*ceil(M/32) CTAs stay within 2.6
  *                  per SM (H = 8 to M = 192, H = 11 to 128, H = 16 to 96 on
- *                  152 SMs); from M = 9 (BF16) or 12 (MXFP8)
+ *                  152 SMs; at H = 8 and 9 <= M <= 32 two chunks of 8 or, for
+ *                  MXFP8, 16 tokens); from M = 9 (BF16) or 12 (MXFP8)
  *                  launched in clusters of the 8 CTAs of a (head, chunk),
  *                  which share x through one TMA multicast per CTA where
  *                  the strides form a tensor map.  Otherwise a tcgen05
