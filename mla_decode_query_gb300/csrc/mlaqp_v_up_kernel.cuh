@@ -161,6 +161,25 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
     __syncthreads();
   }
 
+  // BF16 weights: their wait and the A fragments ahead of the dependency
+  // wait (measured 0.005-0.03 us per layer call faster; for MXFP8 the same
+  // order measured 0.05-0.09 us slower, so its fragments load after it).
+  const int mi = lane >> 3;
+  uint32_t a[4][4];
+  if constexpr (WF == kWeightBF16) {
+    const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
+      pdl_wait();  // exit only after the previous kernel: later waits rely on it
+      return;
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int row = 16 * (4 * warp + s) + 8 * (mi >> 1) + (lane & 7);
+      ldmatrix_x4_trans(a[s], s_w + sw32(row, mi & 1));
+    }
+  }
+
   // 4. Wait for the producer of x (no-op without PDL).
   pdl_wait();
   if constexpr (TRIG == 1) pdl_launch_dependents();
@@ -174,21 +193,15 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_kernel(const __grid_cons
     xv[i] = make_uint4(0u, 0u, 0u, 0u);
     if (m < M) xv[i] = ld_u128(xh + m * p.x_ts + 8 * (c % KC));
   }
-  if constexpr (WF == kWeightBF16) {
-    const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) atomicOr(&g_device_status, kDevStatusWaitTimeout);
-      return;
-    }
-  }
   // A fragments for the warp's four k-steps s = 4w..4w+3: matrices 0/1 =
-  // rows 16s..+7 (columns 0-7 / 8-15), 2/3 = rows 16s+8..+15.
-  const int mi = lane >> 3;
-  uint32_t a[4][4];
+  // rows 16s..+7 (columns 0-7 / 8-15), 2/3 = rows 16s+8..+15.  MXFP8: here,
+  // after the dependency wait; BF16: before it (see there).
+  if constexpr (WF == kWeightMXFP8) {
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int row = 16 * (4 * warp + s) + 8 * (mi >> 1) + (lane & 7);
-    ldmatrix_x4_trans(a[s], s_w + sw32(row, mi & 1));
+    for (int s = 0; s < 4; ++s) {
+      const int row = 16 * (4 * warp + s) + 8 * (mi >> 1) + (lane & 7);
+      ldmatrix_x4_trans(a[s], s_w + sw32(row, mi & 1));
+    }
   }
 #pragma unroll
   for (int i = 0; i < XI; ++i) {
