@@ -207,8 +207,11 @@ int mlaqp_prefetch_weights(const void* weight, const void* weight_scale, int num
                            int weight_format, int pdl, mlaqp_stream_t stream);
 
 /*
- * Launch geometry a run with these arguments uses (for reporting): grid size
- * in CTAs and threads per CTA.  Returns MLAQP_OK or MLAQP_ERR_UNSUPPORTED.
+ * Launch geometry a run with these arguments (nope dim 128) uses on the
+ * current device, for reporting: grid size in CTAs and threads per CTA.
+ * Where the choice depends on the device's SM count (9 <= M <= 32, M > 64)
+ * it queries the device.  Returns MLAQP_OK, MLAQP_ERR_UNSUPPORTED, or the
+ * device query's status (MLAQP_ERR_CUDA without a usable device).
  */
 int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid_ctas,
                        int* threads_per_cta);
