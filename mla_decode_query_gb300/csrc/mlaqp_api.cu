@@ -275,14 +275,21 @@ int cta_chunks(int M) { return (M + mlaqp::kMaxM - 1) / mlaqp::kMaxM; }
 // only H = 8 (to 224 tokens, up to 448 CTAs) and H = 11 (to 160) fit:
 // H = 8, M = 192: BF16 3.64 / 2.42, MXFP8->E4M3 3.60 / 2.78; H = 11,
 // M = 160: 3.74 / 2.65 and 3.62 / 3.02 (tcgen05 / chunks).
-int cta_chunk_cap(int M, int H, int sm_count) {
+// A fourth tier (nope dim 128: 60-62 registers, so four 256-thread CTAs fit
+// an SM; at 192, 80 registers allow three) caps at 4: H = 16, M = 97..128:
+// BF16->E4M3 2.90-2.99 / 2.70-2.78, MXFP8->E4M3 3.32-3.44 / 3.26-3.33;
+// H = 11, M = 161..192: BF16->BF16 3.70 / 2.84-2.90; H = 8, M = 225..256:
+// BF16->BF16 3.64-3.67 / 2.83-2.85, MXFP8->E4M3 3.59-3.67 / 3.28-3.33.
+int cta_chunk_cap(int M, int H, int K, int sm_count) {
   if (M <= kCtaAlwaysM) return 2;
   if (M > kCtaMaxM) return 0;
   const int ctas = mlaqp::kTilesPerHead * H * cta_chunks(M);
-  return ctas <= 2 * sm_count ? 2 : (ctas <= 3 * sm_count ? 3 : 0);
+  if (ctas <= 2 * sm_count) return 2;
+  if (ctas <= 3 * sm_count) return 3;
+  return K == MLAQP_NOPE_DIM && ctas <= 4 * sm_count ? 4 : 0;
 }
 
-bool cta_chunks_fit(int M, int H, int sm_count) { return cta_chunk_cap(M, H, sm_count) != 0; }
+bool cta_chunks_fit(int M, int H, int K, int sm_count) { return cta_chunk_cap(M, H, K, sm_count) != 0; }
 
 // Tokens per chunk of a CTA-tile launch: 32 above M = 32; for 9 <= M <= 32
 // with nope dim 128, 8 (M <= 16) or 16 (MXFP8 weights, M = 17..32) where
@@ -481,7 +488,7 @@ int warp_crossover(int weight_format, int out_dtype, int H) {
 
 // sm_count: the device's SM count (the chunk rules depend on it).
 Arm auto_arm(int weight_format, int out_dtype, int M, int H, int K, int sm_count) {
-  if (M > MLAQP_MAX_M_DECODE) return cta_chunks_fit(M, H, sm_count) ? Arm::kCtaMma : Arm::kTcgen05;
+  if (M > MLAQP_MAX_M_DECODE) return cta_chunks_fit(M, H, K, sm_count) ? Arm::kCtaMma : Arm::kTcgen05;
   if (cta_chunk_len(weight_format, M, H, K, sm_count) != 0) return Arm::kCtaMma;
   if (M < warp_crossover(weight_format, out_dtype, H)) return Arm::kCtaMma;
   if (K != MLAQP_NOPE_DIM && M > 24 && !(weight_format == MLAQP_WEIGHT_BF16 && out_dtype == MLAQP_OUT_E4M3))
@@ -641,7 +648,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
   } else {
     LaunchPolicy pol = launch_policy(a.weight_format, a.out_dtype, M);
     if (M > MLAQP_MAX_M_DECODE && g_policy_trig.load(std::memory_order_relaxed) < 0)
-      pol.cta_cap = cta_chunk_cap(M, H, g_dev[device].sm_count);
+      pol.cta_cap = cta_chunk_cap(M, H, K, g_dev[device].sm_count);
     chunk = cta_chunk_len(a.weight_format, M, H, K, g_dev[device].sm_count);
     k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki, chunk);
     smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
