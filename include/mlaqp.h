@@ -28,8 +28,9 @@
  *     prefill-sized steps that the pages leave to the staged BMM (vLLM PR
  *     #174, sections Safety scope and E2E topology matrix): the decode
  *     (mma.sync) kernel runs in 32-token chunks up to M = 64, and beyond
- *     while its 8*H*ceil(M/32) CTAs fit the device at three per SM (H = 8 to
- *     M = 224, H = 11 to 160, H = 16 to 96 on 152 SMs); otherwise a tcgen05
+ *     while its 8*H*ceil(M/32) CTAs fit the device at four per SM (nope dim
+ *     128; three for 192): H = 8 to M = 256, H = 11 to 192, H = 16 to 128 on
+ *     152 SMs; otherwise a tcgen05
  *     (TMEM-accumulator) kernel takes its place.
  *   - Status codes are the mlaqp_status values; on any non-OK status a
  *     message is available from mlaqp_last_error() on the same thread.
