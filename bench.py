@@ -140,18 +140,15 @@ class LayerSet:
         return [self.q_nope[M], self.q_pe[M]]
 
     def kernel_name(self, M):
-        if self.arm == "tcgen05":
-            return "mlaqp_fused_query_large_kernel"
-        if self.arm == "auto":
-            import mla_decode_query_gb300 as mq
-            st, grid, _ = mq.mlaqp_launch_shape(M, self.H, self.weight_format, self.out_dtype)
-            # the CTA-tile kernel launches 8*H CTAs per token chunk; the warp-tile
-            # kernel's SM-count grid (152) is no multiple of 8*H for H = 8, 11, 16
-            cta = st == 0 and grid % (8 * self.H) == 0
-            if M > 32:
-                return "mlaqp_fused_query_kernel" if cta else "mlaqp_fused_query_large_kernel"
-            return "mlaqp_fused_query_kernel" if cta else "mlaqp_query_warp_kernel"
-        return "mlaqp_fused_query_kernel" if self.arm == "cta_mma" else "mlaqp_query_warp_kernel"
+        """The kernel the library launches for M (its own plan, this device's SM count)."""
+        import torch
+        import mla_decode_query_gb300 as mq
+        st, p = mq.mlaqp_debug_plan(M, self.H, self.weight_format, self.out_dtype, nope_dim=self.K,
+                                    pdl=self.pdl_mode, arm=self.arm,
+                                    sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+        mq.check(st)
+        return {"cta_mma": "mlaqp_fused_query_kernel", "tcgen05": "mlaqp_fused_query_large_kernel"}.get(
+            p["arm"], "mlaqp_query_warp_kernel")
 
     def layer_args(self, M, l):
         io = 0 if self.shared_io else l
@@ -201,9 +198,6 @@ class LayerSet:
         return algorithmic_bytes(M, self.weight_format, self.out_dtype, self.H, self.K)
 
 
-V_MC_MIN_M = {"bf16": 9, "mxfp8": 12}
-
-
 class VLayerSet:
     """L layers of W_UV in one weight format, plus per-M attention outputs x
     and BF16 results laid out [L, M, H, *]; the V up-projection's LayerSet."""
@@ -237,13 +231,14 @@ class VLayerSet:
         return [self.x[M]]
 
     def kernel_name(self, M):
+        """The kernel the library launches for M (its own plan, this device's SM count)."""
         import torch
-        sms = torch.cuda.get_device_properties(0).multi_processor_count
-        ctas = 8 * self.H * -(-M // 32)
-        if M > 64 and 5 * ctas > 13 * sms:  # the library's fit rule (at most 2.6 CTAs per SM)
-            return "mlaqp_v_up_large_kernel"
-        # the library's switch to the x-multicast kernel (BF16 from M = 9, MXFP8 from M = 12)
-        return "mlaqp_v_up_mc_kernel" if M >= V_MC_MIN_M[self.weight_format] else "mlaqp_v_up_kernel"
+        import mla_decode_query_gb300 as mq
+        st, p = mq.mlaqp_debug_v_plan(M, self.H, self.weight_format, pdl=self.pdl_mode,
+                                      sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+        mq.check(st)
+        return {"plain": "mlaqp_v_up_kernel", "multicast": "mlaqp_v_up_mc_kernel"}.get(
+            p["form"], "mlaqp_v_up_large_kernel")
 
     def launch_all(self, M, pdl=True, stream=None):
         import mla_decode_query_gb300 as mq

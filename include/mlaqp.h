@@ -218,6 +218,37 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
                        int* threads_per_cta);
 
 /*
+ * Test hook (no counterpart on the pages): the launch a query call would
+ * make on a device with `sm_count` SMs, computed on the host alone (no
+ * device access), by the same code the run path uses: arm as in
+ * mlaqp_debug_run_arm (MLAQP_ARM_AUTO: the library's choice; the chosen
+ * MLAQP_ARM_* value is returned in *arm_out), the token chunk of a CTA-tile
+ * launch (*chunk_tokens, 0: one launch over all tokens), where a CTA lets the
+ * next kernel launch (*trig: 0 at entry, 1 after the dependency wait -- for
+ * the tcgen05 kernel, after its tensor-memory allocation --, 2 once its
+ * weight tile is ready), the CTAs-per-SM cap the shared-memory padding
+ * imposes (*cta_cap, 0: none; only with pdl != 0), and the grid and block
+ * size.  Any output pointer may be NULL.  Returns MLAQP_OK,
+ * MLAQP_ERR_INVALID_ARG (bad enum, pdl, arm or sm_count) or
+ * MLAQP_ERR_UNSUPPORTED (domain, or a forced arm that does not cover the
+ * call).
+ */
+int mlaqp_debug_plan(int M, int H, int nope_dim, int weight_format, int out_dtype, int pdl, int arm,
+                     int sm_count, int* arm_out, int* chunk_tokens, int* trig, int* cta_cap,
+                     int* grid_ctas, int* threads_per_cta);
+
+/*
+ * Test hook (no counterpart on the pages): as mlaqp_debug_plan, for a V
+ * call with contiguous x: *form 0 = the column-tile kernel reading x with
+ * plain loads, 1 = the x-multicast kernel, 2 = the tcgen05 cluster kernel;
+ * *chunk_tokens = tokens per grid.z chunk; *cluster = CTAs per cluster (1:
+ * none).  Returns MLAQP_OK, MLAQP_ERR_INVALID_ARG or MLAQP_ERR_UNSUPPORTED.
+ */
+int mlaqp_debug_v_plan(int M, int H, int weight_format, int pdl, int sm_count, int* form,
+                       int* chunk_tokens, int* trig, int* cta_cap, int* grid_ctas,
+                       int* threads_per_cta, int* cluster);
+
+/*
  * Device status word (diagnostic, not for the hot path): every in-kernel
  * wait on a copy-completion barrier is bounded in time; a CTA that gives up
  * sets MLAQP_DEVSTATUS_WAIT_TIMEOUT here and returns without writing its

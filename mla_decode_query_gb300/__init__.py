@@ -28,9 +28,11 @@ from .mlaqp import (  # noqa: F401
     load_library,
     mlaqp_can_implement,
     mlaqp_debug_launch_null,
+    mlaqp_debug_plan,
     mlaqp_debug_run_arm,
     mlaqp_debug_set_policy,
     mlaqp_debug_run_bounded_wait,
+    mlaqp_debug_v_plan,
     mlaqp_debug_v_up_bounded_wait,
     mlaqp_device_status,
     mlaqp_last_error,

@@ -499,10 +499,10 @@ Arm auto_arm(int weight_format, int out_dtype, int M, int H, int K, int sm_count
 // Grid of a warp-tile launch: one CTA per SM, but at least 8 CTAs per head
 // (at most kWMaxTilesPerCta tiles per CTA) and at most 32 (one tile each);
 // the kernel splits the CTAs over the heads as evenly as it goes.
-void warp_grid(const DeviceInfo& d, int H, int* ctas, int* tiles_per_cta) {
+void warp_grid(int sm_count, int H, int* ctas, int* tiles_per_cta) {
   const int min_g = H * ((mlaqp::kWTilesPerHead + mlaqp::kWMaxTilesPerCta - 1) / mlaqp::kWMaxTilesPerCta);
   const int max_g = H * mlaqp::kWTilesPerHead;
-  const int g = d.sm_count < min_g ? min_g : (d.sm_count > max_g ? max_g : d.sm_count);
+  const int g = sm_count < min_g ? min_g : (sm_count > max_g ? max_g : sm_count);
   *ctas = g;
   *tiles_per_cta = (mlaqp::kWTilesPerHead + g / H - 1) / (g / H);  // the fewest CTAs a head gets is g / H
 }
@@ -523,14 +523,60 @@ LaunchPolicy warp_launch_policy(int /*weight_format*/, int /*out_dtype*/, int /*
   return LaunchPolicy{0, 2};
 }
 
+// Everything a query call launches, decided from the arguments and the SM
+// count alone (no device access): run_impl, mlaqp_launch_shape and the
+// mlaqp_debug_plan test hook share it.  forced = Arm::kAuto: the library's
+// choice.  Returns MLAQP_ERR_UNSUPPORTED when a forced form does not cover
+// the call.
+struct QueryPlan {
+  Arm arm = Arm::kAuto;
+  const KernelInfo* k = nullptr;
+  LaunchPolicy pol{0, 0};  // mma.sync kernels: trigger point, CTA cap (applied with PDL)
+  int chunk = 0;           // CTA-tile kernel: tokens per grid.z chunk (0: one launch over all tokens)
+  int grid = 0;            // CTAs
+  int threads = 0;         // threads per CTA
+  int tiles_per_cta = 1;   // warp-tile kernel: column tiles per CTA
+};
+
+int plan_query(int weight_format, int out_dtype, int M, int H, int K, int pdl, Arm forced, int sm_count,
+               QueryPlan* q) {
+  *q = QueryPlan{};
+  const int ki = nope_index(K);
+  const Arm arm = forced == Arm::kAuto ? auto_arm(weight_format, out_dtype, M, H, K, sm_count) : forced;
+  if (arm == Arm::kWarpFma && (M > 8 || K != 128))
+    return fail(MLAQP_ERR_UNSUPPORTED, "the CUDA-core arm covers M <= 8 at nope_dim 128");
+  if (arm == Arm::kWarpMma && M > MLAQP_MAX_M_DECODE)
+    return fail(MLAQP_ERR_UNSUPPORTED, "the warp-tile arm covers M <= 32");
+  if (arm == Arm::kCtaMma && M > kCtaMaxM) return fail(MLAQP_ERR_UNSUPPORTED, "the CTA-tile arm covers M <= 256");
+  q->arm = arm;
+  if (arm == Arm::kWarpMma || arm == Arm::kWarpFma) {
+    q->pol = warp_launch_policy(weight_format, out_dtype, M);
+    q->k = lookup_warp(weight_format, out_dtype, M, q->pol.trig, ki, arm == Arm::kWarpFma);
+    warp_grid(sm_count, H, &q->grid, &q->tiles_per_cta);
+    q->threads = q->k->threads * q->tiles_per_cta;
+  } else if (arm == Arm::kTcgen05) {
+    q->k = lookup_large(weight_format, out_dtype, ki, large_tile_index(M), pdl == 2 ? 1 : 0);
+    q->grid = q->k->tiles_per_head * H * large_chunks(M);
+    q->threads = q->k->threads;
+  } else {
+    q->pol = launch_policy(weight_format, out_dtype, M);
+    if (M > MLAQP_MAX_M_DECODE && g_policy_trig.load(std::memory_order_relaxed) < 0)
+      q->pol.cta_cap = cta_chunk_cap(M, H, K, sm_count);
+    q->chunk = cta_chunk_len(weight_format, M, H, K, sm_count);
+    q->k = lookup(weight_format, out_dtype, M, q->pol.trig, ki, q->chunk);
+    q->grid = q->k->tiles_per_head * H * (q->chunk ? (M + q->chunk - 1) / q->chunk : 1);
+    q->threads = q->k->threads;
+  }
+  return MLAQP_OK;
+}
+
 int launch_warp(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long long wait_limit_ns, unsigned extra_tx,
-                Arm arm, int device) {
+                const QueryPlan& q, int device) {
   const int M = a.M, H = a.H, K = a.K;
   const bool mx = a.weight_format == MLAQP_WEIGHT_MXFP8;
-  const LaunchPolicy pol = warp_launch_policy(a.weight_format, a.out_dtype, M);
-  const KernelInfo* k = lookup_warp(a.weight_format, a.out_dtype, M, pol.trig, nope_index(K), arm == Arm::kWarpFma);
-  int ctas = 0, tpc = 0;
-  warp_grid(g_dev[device], H, &ctas, &tpc);
+  const LaunchPolicy pol = q.pol;
+  const KernelInfo* k = q.k;
+  const int ctas = q.grid, tpc = q.tiles_per_cta;
   mlaqp::WarpRunParams params;
   int st = encode_weight_map(&params.wmap, a.weight, H, K, mx, mlaqp::kWTileCols, false, !mx);
   if (st != MLAQP_OK) return st;
@@ -629,30 +675,15 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  Arm arm = forced;
-  if (arm == Arm::kAuto) arm = auto_arm(a.weight_format, a.out_dtype, M, H, K, g_dev[device].sm_count);
-  if (arm == Arm::kWarpFma && (M > 8 || K != 128))
-    return fail(MLAQP_ERR_UNSUPPORTED, "the CUDA-core arm covers M <= 8 at nope_dim 128");
-  if (arm == Arm::kWarpMma && M > MLAQP_MAX_M_DECODE)
-    return fail(MLAQP_ERR_UNSUPPORTED, "the warp-tile arm covers M <= 32");
-  if (arm == Arm::kCtaMma && M > kCtaMaxM) return fail(MLAQP_ERR_UNSUPPORTED, "the CTA-tile arm covers M <= 256");
-  if (arm == Arm::kWarpMma || arm == Arm::kWarpFma) return launch_warp(a, stream, pdl, wait_limit_ns, extra_tx, arm, device);
+  QueryPlan q;
+  st = plan_query(a.weight_format, a.out_dtype, M, H, K, pdl, forced, g_dev[device].sm_count, &q);
+  if (st != MLAQP_OK) return st;
+  if (q.arm == Arm::kWarpMma || q.arm == Arm::kWarpFma) return launch_warp(a, stream, pdl, wait_limit_ns, extra_tx, q, device);
 
-  const bool large = arm == Arm::kTcgen05;
-  const KernelInfo* k = nullptr;
-  int smem_bytes = 0;
-  int chunk = 0;  // tokens per chunk of a CTA-tile launch (0: one launch over all M)
-  if (large) {
-    k = lookup_large(a.weight_format, a.out_dtype, ki, large_tile_index(M), pdl == 2 ? 1 : 0);
-    smem_bytes = large_smem(g_dev[device], k->smem_bytes, M);
-  } else {
-    LaunchPolicy pol = launch_policy(a.weight_format, a.out_dtype, M);
-    if (M > MLAQP_MAX_M_DECODE && g_policy_trig.load(std::memory_order_relaxed) < 0)
-      pol.cta_cap = cta_chunk_cap(M, H, K, g_dev[device].sm_count);
-    chunk = cta_chunk_len(a.weight_format, M, H, K, g_dev[device].sm_count);
-    k = lookup(a.weight_format, a.out_dtype, M, pol.trig, ki, chunk);
-    smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
-  }
+  const bool large = q.arm == Arm::kTcgen05;
+  const KernelInfo* k = q.k;
+  const int smem_bytes = large ? large_smem(g_dev[device], k->smem_bytes, M)
+                               : smem_for_cap(g_dev[device], k->smem_bytes, pdl ? q.pol.cta_cap : 0);
   RunParams params;
   st = encode_weight_map(&params.wmap, a.weight, H, K, mx, mlaqp::kNTile, !mx);
   if (st != MLAQP_OK) return st;
@@ -673,7 +704,7 @@ int run_impl(const RunArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lon
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(k->tiles_per_head), static_cast<unsigned>(H),
-                     static_cast<unsigned>(large ? large_chunks(M) : (chunk ? (M + chunk - 1) / chunk : 1)));
+                     static_cast<unsigned>(large ? large_chunks(M) : (q.chunk ? (M + q.chunk - 1) / q.chunk : 1)));
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -817,6 +848,42 @@ struct VUpArgs {
   int M, H, weight_format;
 };
 
+// Everything a V call launches, decided from the arguments and the SM count
+// alone (no device access): v_up_impl and the mlaqp_debug_v_plan test hook
+// share it.  multicast_ok: whether x's strides form the tensor map the
+// x-multicast kernel reads (v_up_impl plans again without it when not).
+struct VPlan {
+  int form = 0;            // 0 column-tile kernel, plain loads; 1 x multicast; 2 tcgen05 cluster kernel
+  const KernelInfo* k = nullptr;
+  LaunchPolicy pol{0, 0};  // column-tile kernels: trigger point, CTA cap (applied with PDL)
+  int chunk = 0;           // tokens per grid.z chunk
+  int chunks = 1;          // grid.z
+  int tt = 0;              // token rows of a CTA's tile (multicast box height, cluster token tile)
+};
+
+void plan_v(int weight_format, int M, int H, int pdl, int sm_count, bool multicast_ok, VPlan* v) {
+  *v = VPlan{};
+  if (!v_chunks_fit(M, H, sm_count)) {
+    v->form = 2;
+    v->k = lookup_v_up_large(weight_format, M, pdl == 2 ? 1 : 0);
+    v->tt = mlaqp::kVLargeTokTiles[v_large_tile_index(M)];
+    v->chunk = v->tt;
+    v->chunks = (M + v->tt - 1) / v->tt;
+    return;
+  }
+  v->pol = v_up_launch_policy(weight_format, M);
+  if (v->pol.cta_cap != 0 && M >= kVLargeMinM) v->pol.cta_cap = v_chunk_cap(M, H, sm_count);
+  const int trig = v->pol.trig == 0 ? 0 : 1;
+  const int vch = v_small_chunk(weight_format, M, H, sm_count);
+  const int cm = vch ? vch : (M < mlaqp::kVChunk ? M : mlaqp::kVChunk);  // tokens per CTA chunk
+  v->tt = 8 * ((cm + 7) / 8);
+  // 8-token chunks read x with plain loads (x is 8 KB per CTA there)
+  v->form = multicast_ok && vch != 8 && M >= v_mc_min_m(weight_format) ? 1 : 0;
+  v->k = v->form == 1 ? lookup_v_up_mc(weight_format, cm, trig) : lookup_v_up(weight_format, cm, trig);
+  v->chunk = vch ? vch : mlaqp::kVChunk;
+  v->chunks = vch ? (M + vch - 1) / vch : v_up_chunks(M);
+}
+
 int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long long wait_limit_ns, unsigned extra_tx) {
   if (pdl < 0 || pdl > 2) return fail(MLAQP_ERR_INVALID_ARG, "pdl must be 0, 1 or 2");
   const int M = a.M, H = a.H;
@@ -855,32 +922,18 @@ int v_up_impl(const VUpArgs& a, mlaqp_stream_t stream, int pdl, unsigned long lo
   st = check_device(device);
   if (st != MLAQP_OK) return st;
 
-  const bool large = !v_chunks_fit(M, H, g_dev[device].sm_count);
-  const KernelInfo* k = nullptr;
-  int smem_bytes = 0;
-  int chunks = 0;
-  if (large) {
-    k = lookup_v_up_large(a.weight_format, M, pdl == 2 ? 1 : 0);
-    const int tt = mlaqp::kVLargeTokTiles[v_large_tile_index(M)];
-    chunks = (M + tt - 1) / tt;
-    smem_bytes = tmem_safe_smem(g_dev[device], k->smem_bytes, ((M < tt ? M : tt) + 15) & ~15);
-  }
   mlaqp::VUpParams params;
-  bool mc = false;
-  if (!large) {
-    LaunchPolicy pol = v_up_launch_policy(a.weight_format, M);
-    if (pol.cta_cap != 0 && M >= kVLargeMinM) pol.cta_cap = v_chunk_cap(M, H, g_dev[device].sm_count);
-    const int trig = pol.trig == 0 ? 0 : 1;
-    const int vch = v_small_chunk(a.weight_format, M, H, g_dev[device].sm_count);
-    const int cm = vch ? vch : (M < mlaqp::kVChunk ? M : mlaqp::kVChunk);  // tokens per CTA chunk
-    const int tt = 8 * ((cm + 7) / 8);
-    // 8-token chunks read x with plain loads (x is 8 KB per CTA there)
-    mc = vch != 8 && M >= v_mc_min_m(a.weight_format) &&
-         encode_v_x_map(&params.xmap, a.x, a.x_ts, a.x_hs, M, H, tt);
-    k = mc ? lookup_v_up_mc(a.weight_format, cm, trig) : lookup_v_up(a.weight_format, cm, trig);
-    chunks = vch ? (M + vch - 1) / vch : v_up_chunks(M);
-    smem_bytes = smem_for_cap(g_dev[device], k->smem_bytes, pdl ? pol.cta_cap : 0);
-  }
+  const int sm_count = g_dev[device].sm_count;
+  VPlan v;
+  plan_v(a.weight_format, M, H, pdl, sm_count, true, &v);
+  if (v.form == 1 && !encode_v_x_map(&params.xmap, a.x, a.x_ts, a.x_hs, M, H, v.tt))
+    plan_v(a.weight_format, M, H, pdl, sm_count, false, &v);
+  const bool large = v.form == 2;
+  const bool mc = v.form == 1;
+  const KernelInfo* k = v.k;
+  const int chunks = v.chunks;
+  const int smem_bytes = large ? tmem_safe_smem(g_dev[device], k->smem_bytes, ((M < v.tt ? M : v.tt) + 15) & ~15)
+                               : smem_for_cap(g_dev[device], k->smem_bytes, pdl ? v.pol.cta_cap : 0);
   st = encode_v_weight_map(&params.wmap, a.weight, H, mx, large);
   if (st != MLAQP_OK) return st;
   params.x = static_cast<const uint16_t*>(a.x);
@@ -1042,31 +1095,50 @@ int mlaqp_launch_shape(int M, int H, int weight_format, int out_dtype, int* grid
       return st;
     }
   }
-  const Arm arm = auto_arm(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM, sm_count);
-  if (arm == Arm::kTcgen05) {
-    const KernelInfo* k = lookup_large(weight_format, out_dtype, 0, large_tile_index(M));
-    if (grid_ctas) *grid_ctas = k->tiles_per_head * H * large_chunks(M);
-    if (threads_per_cta) *threads_per_cta = k->threads;
-    return MLAQP_OK;
-  }
-  if (arm == Arm::kCtaMma) {
-    const int chunk = cta_chunk_len(weight_format, M, H, MLAQP_NOPE_DIM, sm_count);
-    const KernelInfo* k =
-        lookup(weight_format, out_dtype, M, launch_policy(weight_format, out_dtype, M).trig, 0, chunk);
-    if (grid_ctas) *grid_ctas = k->tiles_per_head * H * (chunk ? (M + chunk - 1) / chunk : 1);
-    if (threads_per_cta) *threads_per_cta = k->threads;
-    return MLAQP_OK;
-  }
-  int dev = 0;
-  int st = resolve_device(-1, &dev);
+  QueryPlan q;
+  const int st = plan_query(weight_format, out_dtype, M, H, MLAQP_NOPE_DIM, 1, Arm::kAuto, sm_count, &q);
   if (st != MLAQP_OK) return st;
-  st = check_device(dev);
+  if (grid_ctas) *grid_ctas = q.grid;
+  if (threads_per_cta) *threads_per_cta = q.threads;
+  return MLAQP_OK;
+}
+
+int mlaqp_debug_plan(int M, int H, int nope_dim, int weight_format, int out_dtype, int pdl, int arm, int sm_count,
+                     int* arm_out, int* chunk_tokens, int* trig, int* cta_cap, int* grid_ctas, int* threads_per_cta) {
+  if (!valid_enums(weight_format, out_dtype)) return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format or out_dtype");
+  if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M || nope_index(nope_dim) < 0)
+    return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H, M or nope_dim");
+  if (pdl < 0 || pdl > 2 || arm < MLAQP_ARM_AUTO || arm > MLAQP_ARM_TCGEN05 || sm_count < 1)
+    return fail(MLAQP_ERR_INVALID_ARG, "pdl must be 0..2, arm a MLAQP_ARM_* value and sm_count >= 1");
+  QueryPlan q;
+  const int st = plan_query(weight_format, out_dtype, M, H, nope_dim, pdl, static_cast<Arm>(arm), sm_count, &q);
   if (st != MLAQP_OK) return st;
-  const KernelInfo* k = lookup_warp(weight_format, out_dtype, M, 0, 0, false);
-  int ctas = 0, tpc = 0;
-  warp_grid(g_dev[dev], H, &ctas, &tpc);
-  if (grid_ctas) *grid_ctas = ctas;
-  if (threads_per_cta) *threads_per_cta = k->threads * tpc;
+  const bool tc = q.arm == Arm::kTcgen05;
+  if (arm_out) *arm_out = static_cast<int>(q.arm);
+  if (chunk_tokens) *chunk_tokens = q.chunk;
+  if (trig) *trig = tc ? (pdl == 2 ? 0 : 1) : q.pol.trig;
+  if (cta_cap) *cta_cap = (pdl && !tc) ? q.pol.cta_cap : 0;
+  if (grid_ctas) *grid_ctas = q.grid;
+  if (threads_per_cta) *threads_per_cta = q.threads;
+  return MLAQP_OK;
+}
+
+int mlaqp_debug_v_plan(int M, int H, int weight_format, int pdl, int sm_count, int* form, int* chunk_tokens,
+                       int* trig, int* cta_cap, int* grid_ctas, int* threads_per_cta, int* cluster) {
+  if (weight_format != MLAQP_WEIGHT_BF16 && weight_format != MLAQP_WEIGHT_MXFP8)
+    return fail(MLAQP_ERR_INVALID_ARG, "unknown weight_format");
+  if (!supported_heads(H) || M < 1 || M > MLAQP_MAX_M) return fail(MLAQP_ERR_UNSUPPORTED, "unsupported H or M");
+  if (pdl < 0 || pdl > 2 || sm_count < 1) return fail(MLAQP_ERR_INVALID_ARG, "pdl must be 0..2 and sm_count >= 1");
+  VPlan v;
+  plan_v(weight_format, M, H, pdl, sm_count, true, &v);
+  const bool tc = v.form == 2;
+  if (form) *form = v.form;
+  if (chunk_tokens) *chunk_tokens = v.chunk;
+  if (trig) *trig = tc ? (pdl == 2 ? 0 : 1) : v.pol.trig;
+  if (cta_cap) *cta_cap = (pdl && !tc) ? v.pol.cta_cap : 0;
+  if (grid_ctas) *grid_ctas = v.k->tiles_per_head * H * v.chunks;
+  if (threads_per_cta) *threads_per_cta = v.k->threads;
+  if (cluster) *cluster = v.form == 0 ? 1 : v.k->tiles_per_head;
   return MLAQP_OK;
 }
 

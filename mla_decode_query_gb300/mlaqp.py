@@ -65,6 +65,8 @@ _SIGNATURES = {
     "mlaqp_prefetch_weights": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p]),
     "mlaqp_launch_shape": (_c_int, [_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_int),
                                     ctypes.POINTER(_c_int)]),
+    "mlaqp_debug_plan": (_c_int, [_c_int] * 8 + [ctypes.POINTER(_c_int)] * 6),
+    "mlaqp_debug_v_plan": (_c_int, [_c_int] * 5 + [ctypes.POINTER(_c_int)] * 7),
     "mlaqp_device_status": (_c_int, [ctypes.POINTER(ctypes.c_uint), _c_int]),
     "mlaqp_debug_run_bounded_wait": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                               ctypes.c_int64, _c_void_p, _c_int, _c_int, _c_int, _c_int,
@@ -242,6 +244,39 @@ def mlaqp_launch_shape(M, H, weight_format="bf16", out_dtype="bf16"):
     st = load_library().mlaqp_launch_shape(int(M), int(H), _fmt(weight_format, WEIGHT_FORMATS),
                                            _fmt(out_dtype, OUT_DTYPES), ctypes.byref(g), ctypes.byref(t))
     return st, g.value, t.value
+
+
+ARM_NAMES = {v: k for k, v in ARMS.items()}
+
+
+def mlaqp_debug_plan(M, H, weight_format="bf16", out_dtype="bf16", nope_dim=128, pdl=1, arm="auto", sm_count=152):
+    """The launch a query call would make on a device with ``sm_count`` SMs
+    (host-side, no device).  Returns ``(status, plan)`` with plan a dict:
+    arm (name), chunk_tokens, trig, cta_cap, grid_ctas, threads_per_cta."""
+    out = [_c_int(0) for _ in range(6)]
+    st = load_library().mlaqp_debug_plan(int(M), int(H), int(nope_dim), _fmt(weight_format, WEIGHT_FORMATS),
+                                         _fmt(out_dtype, OUT_DTYPES), int(pdl), _fmt(arm, ARMS), int(sm_count),
+                                         *[ctypes.byref(o) for o in out])
+    keys = ("arm", "chunk_tokens", "trig", "cta_cap", "grid_ctas", "threads_per_cta")
+    plan = {k: o.value for k, o in zip(keys, out)}
+    plan["arm"] = ARM_NAMES.get(plan["arm"], plan["arm"])
+    return st, plan
+
+
+V_FORMS = {0: "plain", 1: "multicast", 2: "cluster"}
+
+
+def mlaqp_debug_v_plan(M, H, weight_format="bf16", pdl=1, sm_count=152):
+    """As mlaqp_debug_plan for a V call with contiguous x.  Returns
+    ``(status, plan)``: form (plain / multicast / cluster), chunk_tokens,
+    trig, cta_cap, grid_ctas, threads_per_cta, cluster."""
+    out = [_c_int(0) for _ in range(7)]
+    st = load_library().mlaqp_debug_v_plan(int(M), int(H), _fmt(weight_format, WEIGHT_FORMATS), int(pdl),
+                                           int(sm_count), *[ctypes.byref(o) for o in out])
+    keys = ("form", "chunk_tokens", "trig", "cta_cap", "grid_ctas", "threads_per_cta", "cluster")
+    plan = {k: o.value for k, o in zip(keys, out)}
+    plan["form"] = V_FORMS.get(plan["form"], plan["form"])
+    return st, plan
 
 
 def mlaqp_device_status(reset=False):

@@ -279,3 +279,17 @@ def test_dependent_chain_reads_previous_output(cuda_device, with_prefetch):
         torch.cuda.synchronize()
         for l in range(L):
             np.testing.assert_array_equal(_rows(outs[l], M, H, row, "bf16"), refs[l], err_msg=f"replay {rep} layer {l}")
+
+
+def test_plan_matches_launch_shape_on_this_device(cuda_device):
+    # The host-side plan (tests/test_plan_host.py pins its rules) at this
+    # device's SM count is the launch the library reports and makes.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for fmt, od in PAIRS:
+        for h in (8, 11, 16):
+            for m in (1, 8, 9, 16, 17, 24, 32, 33, 64, 65, 96, 128, 129, 160, 192, 224, 256):
+                st, grid, threads = mq.mlaqp_launch_shape(m, h, fmt, od)
+                assert st == mq.MLAQP_OK, mq.mlaqp_last_error()
+                st, p = mq.mlaqp_debug_plan(m, h, fmt, od, sm_count=sms)
+                assert st == mq.MLAQP_OK
+                assert (p["grid_ctas"], p["threads_per_cta"]) == (grid, threads), (fmt, od, h, m, p)
