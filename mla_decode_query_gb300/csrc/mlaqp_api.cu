@@ -89,8 +89,9 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
-// Bit (wf*2+od)*4 + (mt-1) set once that decode specialisation's image is
-// loaded; bit 16 + wf*2+od for the large-M kernels.
+// Bit (wf*2+od)*4 + (mt-1) set once that decode specialisation's images are
+// loaded; bit 16 + wf*2+od for the M > 32 kernels (tcgen05 and the
+// 32-token chunked CTA-tile form).
 std::atomic<uint32_t> g_prewarmed[kMaxDevices];
 std::mutex g_prewarm_mutex;
 
@@ -204,7 +205,7 @@ int encode_weight_map(CUtensorMap* map, const void* weight, int H, int K, bool m
 // one.  Against the earlier mix (cap 3 up to M = 8, MXFP8 uncapped up to
 // M = 4, trigger after the wait above M = 16), MXFP8->E4M3 went from
 // 1.62 / 1.82 / 2.84 us to 1.38 / 1.52 / 2.54 us at M = 1 / 8 / 32.  The
-// exception is BF16 weights with E4M3 output above M = 16, which trigger
+// exception is BF16 weights with E4M3 output at M = 17..32, which trigger
 // after the wait (2.16 against 2.61 us at M = 32).  The V up-projection
 // (x-multicast kernel from M = 9) likewise triggers after the wait for BF16
 // weights at 17 <= M <= 32 (2.12 against 2.37 us at M = 32), and drops the
@@ -254,8 +255,8 @@ int nope_index(int K) {
 // Above M = 32 the CTA-tile kernel runs in 32-token chunks (grid.z; the
 // later chunks find the weight tile in L2) instead of the tcgen05 kernel:
 // always up to M = 64, and up to kCtaMaxM while all its CTAs fit on the GPU
-// at two, else three, per SM (cta_chunk_cap).  It needs no tensor memory, so it may trigger the next
-// launch at entry.  Measured on GB300 (128/256-layer PDL chains, pdl = 1, us
+// at two, three or (nope dim 128) four per SM (cta_chunk_cap).  It needs no
+// tensor memory, so it may trigger the next launch at entry.  Measured on GB300 (128/256-layer PDL chains, pdl = 1, us
 // per layer call, tcgen05 / chunked): H = 16, BF16->BF16 2.43 / 2.08 at
 // M = 33 and 2.51 / 2.28 at 64; MXFP8->E4M3 3.22 / 2.43 and 3.34 / 2.52;
 // BF16->E4M3 2.46 / 2.12 and 2.55 / 2.27 (entry trigger, cap 2; after-wait
@@ -462,9 +463,10 @@ RunArgs contiguous_args(const void* q_nope, const void* q_pe, const void* weight
                  weight, weight_scale, out, out_row_stride, q_scale, M, H, MLAQP_NOPE_DIM, weight_format, out_dtype};
 }
 
-// Which kernel serves a layer call.  kAuto is the library's choice (the
-// warp-tile tensor-core kernel up to M = 32, the tcgen05 kernel above); the
-// others force one form, for measurement (mlaqp_debug_run_arm).
+// Which kernel serves a layer call.  kAuto is the library's choice
+// (auto_arm: the CTA-tile kernel, whole or in token chunks, the warp-tile
+// kernel, or the tcgen05 kernel); the others force one form, for
+// measurement (mlaqp_debug_run_arm).
 enum class Arm : int { kAuto = 0, kWarpMma = 1, kWarpFma = 2, kCtaMma = 3, kTcgen05 = 4 };
 
 // The library's kernel choice for a decode call (M <= 32), from 128-layer
@@ -479,7 +481,8 @@ enum class Arm : int { kAuto = 0, kWarpMma = 1, kWarpFma = 2, kCtaMma = 3, kTcge
 // M = 13 (MXFP8 -> BF16, BF16 -> E4M3), 15 (BF16 -> BF16), 16 (MXFP8 ->
 // E4M3).  Nope dim 192 (H = 16): the warp-tile kernel from M = 17, but for
 // M = 25..32 (four token tiles, 12 k-steps) only with BF16 weights and E4M3
-// output.  Above 32 tokens: the tcgen05 kernel.
+// output.  Above 32 tokens: the chunked CTA-tile kernel while its CTAs fit,
+// else the tcgen05 kernel (cta_chunk_cap).
 int warp_crossover(int weight_format, int out_dtype, int H) {
   if (H > 8) return 17;
   if (weight_format == MLAQP_WEIGHT_BF16) return out_dtype == MLAQP_OUT_BF16 ? 15 : 13;
