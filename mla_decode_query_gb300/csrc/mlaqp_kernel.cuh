@@ -251,18 +251,6 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float hi, float lo) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// E4M3 pair -> FP32 pair, exactly: every E4M3 value (subnormals included) is
-// a normal FP16 value, so the E4M3x2 -> F16x2 conversion is exact, as is
-// F16 -> F32.  Byte 0 of `pair16` gives `lo`.
-__device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair16, float& lo, float& hi) {
-  uint32_t h2;
-  const uint16_t p16 = static_cast<uint16_t>(pair16);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(p16));
-  const uint16_t h_lo = static_cast<uint16_t>(h2), h_hi = static_cast<uint16_t>(h2 >> 16);
-  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(h_lo));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(h_hi));
-}
-
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -282,12 +270,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two) {
 // 2^(x-7) as a BF16 bit pattern, for an E8M0 byte x <= 134 (exponent field
 // x + 120 stays below 255).
 __device__ __forceinline__ uint32_t pow2_bf16(uint32_t x) { return (x + 120u) << 7; }
-
-// E8M0 byte -> 2^(x-127) as FP32 (x = 0 is the subnormal 2^-127, 255 NaN).
-__device__ __forceinline__ float e8m0_to_f32(uint32_t x) {
-  const uint32_t bits = x == 0 ? 0x00400000u : (x == 255 ? 0x7FC00000u : (x << 23));
-  return __uint_as_float(bits);
-}
 
 // a / q_scale for a BF16 value `a` (bits), as far as the E4M3 conversion
 // that follows can tell: the result converts to the same E4M3 code as the
@@ -548,6 +530,30 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   }
   __syncthreads();  // barrier initialised before anyone waits on it
 
+  // E4M3 output: table of RN((128+f)/q_scale) and the per-significand check
+  // of the one-multiply form, one significand per thread (both uniform
+  // across the grid: q_scale is one value), published and combined by a CTA
+  // barrier.  The 32-token chunked form builds it here, while the weight
+  // copy is in flight, and lets the barrier after the MXFP8 dequantisation
+  // combine it (MXFP8->E4M3, H = 16, M = 40 / 64 / 96: 2.37 / 2.43 / 2.74
+  // against 2.47 / 2.54 / 2.87 us per layer call); the other forms build it
+  // after the dequantisation (there the early table measured 0.01-0.04 us
+  // slower).
+  constexpr bool kEarlyTable = CH && MT == 4;
+  uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L::Div);
+  bool table_ok = false, mul_ok = false, mine = false;
+  float rcp = 1.f;
+  auto build_table = [&]() {
+    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;
+    rcp = __frcp_rn(qs);
+    mine = table_ok;
+    if (table_ok && tid < 128) {
+      divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
+      mine = e4m3_mul_exact_for(tid, qs, rcp);
+    }
+  };
+  if constexpr (OD == kOutE4M3 && kEarlyTable) build_table();
+
   // 3. MXFP8: dequantise into the swizzled BF16 tile before the dependency
   //    wait.  Job (row k, chunk c of 8 columns); 8K jobs, 8K/(128 TS) per thread.
   if constexpr (WF == kWeightMXFP8) {
@@ -593,7 +599,11 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
       const int k = (tid >> 3) + (kCta / 8) * i;
       *reinterpret_cast<uint4*>(smem + L::A + sw128(k, c)) = make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
     }
-    __syncthreads();
+    if constexpr (OD == kOutE4M3 && kEarlyTable) {
+      mul_ok = __syncthreads_and(mine);  // also publishes the table
+    } else {
+      __syncthreads();
+    }
     if constexpr (TRIG == 2) pdl_launch_dependents();
   } else if constexpr (TRIG == 2) {
     const bool ok = mbar_wait_bounded(s_bar, 0, p.wait_limit_ns);
@@ -604,21 +614,8 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
     }
     pdl_launch_dependents();
   }
-
-  // E4M3 output: table of RN((128+f)/q_scale) and the per-significand check
-  // of the one-multiply form, one significand per thread (both uniform
-  // across the grid: q_scale is one value).
-  uint32_t* divtab = reinterpret_cast<uint32_t*>(smem + L::Div);
-  bool table_ok = false, mul_ok = false;
-  float rcp = 1.f;
-  if constexpr (OD == kOutE4M3) {
-    table_ok = qs >= 0x1p-100f && qs <= 0x1p100f;
-    rcp = __frcp_rn(qs);
-    bool mine = table_ok;
-    if (table_ok && tid < 128) {
-      divtab[tid] = __float_as_uint(__fdiv_rn(static_cast<float>(128 + tid), qs));
-      mine = e4m3_mul_exact_for(tid, qs, rcp);
-    }
+  if constexpr (OD == kOutE4M3 && !(kEarlyTable && WF == kWeightMXFP8)) {
+    if constexpr (!kEarlyTable) build_table();
     mul_ok = __syncthreads_and(mine);  // also publishes the table
   }
 

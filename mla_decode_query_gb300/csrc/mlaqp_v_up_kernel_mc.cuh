@@ -189,9 +189,12 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_mc_kernel(const __grid_c
   //    m*128 + 16*(c ^ m%8)): chunk 4*s2 + mi of tokens 8jt..8jt+7 gives
   //    b0/b1 of steps 2*s2 and 2*s2+1 of this warp.
   const uint32_t s_box = s_x + warp * (TT * 128);
-  float acc[MT][4];
+  constexpr int NC = MT <= 2 ? 2 : 1;  // accumulator chains, as in mlaqp_v_up_kernel.cuh
+  float acc[NC][MT][4];
 #pragma unroll
-  for (int jt = 0; jt < MT; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.f;
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int jt = 0; jt < MT; ++jt) acc[c][jt][0] = acc[c][jt][1] = acc[c][jt][2] = acc[c][jt][3] = 0.f;
 #pragma unroll
   for (int s2 = 0; s2 < 2; ++s2) {
     uint32_t b[MT][4];
@@ -202,9 +205,15 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_mc_kernel(const __grid_c
     }
 #pragma unroll
     for (int jt = 0; jt < MT; ++jt) {
-      mma_bf16_16816(acc[jt], a[2 * s2], b[jt][0], b[jt][1]);
-      mma_bf16_16816(acc[jt], a[2 * s2 + 1], b[jt][2], b[jt][3]);
+      mma_bf16_16816(acc[0][jt], a[2 * s2], b[jt][0], b[jt][1]);
+      mma_bf16_16816(acc[NC - 1][jt], a[2 * s2 + 1], b[jt][2], b[jt][3]);
     }
+  }
+  if constexpr (NC == 2) {
+#pragma unroll
+    for (int jt = 0; jt < MT; ++jt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[0][jt][e] += acc[1][jt][e];
   }
 
   // 7. Cross-warp sum (as in mlaqp_v_up_kernel.cuh): partial (jt, e, lane) of
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(kVThreads) mlaqp_v_up_mc_kernel(const __grid_c
 #pragma unroll
   for (int jt = 0; jt < MT; ++jt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) red[((warp * MT + jt) * 4 + e) * kVRedRow + lane] = acc[jt][e];
+    for (int e = 0; e < 4; ++e) red[((warp * MT + jt) * 4 + e) * kVRedRow + lane] = acc[0][jt][e];
   __syncthreads();
   if (tid < 64 * MT) {
     const int t4 = tid & 3;
