@@ -566,7 +566,11 @@ def run_gpu(args):
     roof = {"bound": "hbm", "kernel": f"{' + '.join(kernel_names)} ({dominant})",
             "achieved": round(ach, 1), "peak": peaks[0], "unit": "GB/s",
             "frac": round(ach / peaks[0], 4), "peak_source": peaks[1], "traffic": traffic,
-            "traffic_source": TRAFFIC_FILE if traffic else "kernel changed since the last ncu capture",
+            "traffic_source": (TRAFFIC_FILE if traffic else
+                               "no committed per-launch ncu table for this workload (the query op, K=128, H=16, "
+                               "M in {1,2,4,8,16,32} has one)" if (v_up or args.nope != 128 or heads != (16,)
+                                                                  or not all(M in M_POINTS for _, M in dom_points))
+                               else "kernel changed since the last ncu capture"),
             "algorithmic_bytes_per_launch": round(kern_bytes[dominant] / (args.steps * sum(s.L for s, _ in dom_points))),
             "per_kernel_gbs": {f: round(kern_bytes[f] / (kern_ms[f] * 1e-3) / 1e9, 1) for f in kern_ms}}
     floor = launch_floor(args.steps, args.warmup)
