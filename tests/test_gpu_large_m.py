@@ -226,10 +226,13 @@ def test_bounded_wait_reports_timeout_and_frees_tmem(cuda_device, H, M):
         assert word == 0
 
 
+@pytest.mark.parametrize("M", [96, 160])
 @pytest.mark.parametrize("qs", [1e-3, 2.0 ** -110, 2.0 ** 110])
-def test_e4m3_saturation_and_plain_division(cuda_device, qs):
-    # Saturation to 448, and q_scale outside the table range (plain division).
-    H, M = 16, 96
+def test_e4m3_saturation_and_plain_division(cuda_device, qs, M):
+    # Saturation to 448, and q_scale outside the table range (plain division),
+    # in the chunked CTA-tile kernel (M = 96, three chunks) and the tcgen05
+    # kernel (M = 160).
+    H = 16
     d = inputs.make_layer(inputs.layer_seed(37, 0), H, "mxfp8", m_max=M)
     qs = np.float32(qs)
     got = _rows(_run(_dev(d), M, H, "mxfp8", "e4m3", qs), M, H, D * H, "e4m3")
@@ -239,9 +242,11 @@ def test_e4m3_saturation_and_plain_division(cuda_device, qs):
 
 @pytest.mark.parametrize("K", [128, 192])
 def test_strided_and_head_major_inputs(cuda_device, K):
-    # The tcgen05 kernel reads q_nope / q_pe through token and head strides:
-    # views into the upstream [M, H, K+64] projection, and a head-major
-    # [H, M, K] q_nope with a head-major [H, M, 64] q_pe.
+    # The kernels above 32 tokens (H = 16: the chunked CTA-tile kernel at
+    # M = 33 and 100, the tcgen05 kernel at 256) read q_nope / q_pe through
+    # token and head strides: views into the upstream [M, H, K+64]
+    # projection, and a head-major [H, M, K] q_nope with a head-major
+    # [H, M, 64] q_pe.
     H = 16
     for fmt, od in (("bf16", "bf16"), ("mxfp8", "e4m3")):
         d = inputs.make_layer(inputs.layer_seed(38, K), H, fmt, m_max=M_MAX, nope=K)

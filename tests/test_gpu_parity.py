@@ -191,7 +191,7 @@ def test_bounded_wait_reports_timeout_and_writes_nothing(cuda_device):
 
 
 @pytest.mark.parametrize("M,arm", [(8, "auto"), (32, "auto"), (64, "auto"), (8, "cta_mma"), (32, "cta_mma"),
-                                   (4, "warp_fma")])
+                                   (4, "warp_fma"), (64, "tcgen05")])
 @pytest.mark.parametrize("qs", [0.01, 0.0371, 0.1, 3.0, 1e-20, 1e20, 2.0 ** -110, 2.0 ** 110,
                                 0.012109374627470970, 0.02734375])
 def test_e4m3_division_every_bf16_value(cuda_device, qs, M, arm):
@@ -202,9 +202,10 @@ def test_e4m3_division_every_bf16_value(cuda_device, qs, M, arm):
     # per-CTA check for most scales) and their table fallback (the last two
     # scales, for which the check refuses: one multiply by RN(1/q_scale)
     # would get 32 and 60 BF16 values' codes wrong); the CTA-tile kernel's
-    # table (M = 8) and checked-multiply (M = 32) forms; the tcgen05 kernel
-    # (M = 64); results that overflow or underflow binary32; and q_scale
-    # outside 2^-100..2^100 (plain division).
+    # table (M = 8) and checked-multiply (M = 32) forms; its 32-token chunked
+    # form, which builds the table before its weight wait (M = 64); the
+    # tcgen05 kernel (M = 64, forced); results that overflow or underflow
+    # binary32; and q_scale outside 2^-100..2^100 (plain division).
     H = 16
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # drop inf / NaN patterns

@@ -2,8 +2,8 @@
 
 Each query call draws M (spread over 1..256, so that every kernel form and
 its boundaries are crossed: the CTA-tile and warp-tile decode kernels, the
-chunked CTA-tile kernel at two and three CTAs per SM, the tcgen05 kernel),
-H, the nope dim, the format pair, the q_nope / q_pe layout (contiguous,
+chunked CTA-tile kernel at two, three and four CTAs per SM, the tcgen05
+kernel), H, the nope dim, the format pair, the q_nope / q_pe layout (contiguous,
 views of the upstream [M,H,K+64] projection, head-major q_nope), a pitched
 output with canaries in the padding and the pdl mode, and compares the
 result with the oracle: q_pe bit-exact, the BF16 projection within its
