@@ -178,12 +178,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// The TMA unit fetches `bytes` (a multiple of 16, from a 16-byte aligned
-// address) into L2; nothing waits for it.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint32_t ld_u32(const void* p) {
   uint32_t v;
   asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -519,9 +513,9 @@ __global__ void __launch_bounds__(kThreads * TS) mlaqp_fused_query_kernel(const 
   // 2. Warm L2 with the head's q rows (L2 is the coherence point, so a line
   //    fetched before the producer writes it is updated by that write; the
   //    values themselves are read only after the dependency wait), one
-  //    prefetch per 128-byte line (a bulk prefetch per row, as in the
-  //    warp-tile kernel, measured no faster up to M = 32 and 0.06-0.35 us
-  //    slower per layer call in the chunked forms above).
+  //    prefetch per 128-byte line (a bulk prefetch per row measured no
+  //    faster up to M = 32 and 0.06-0.35 us slower per layer call in the
+  //    chunked forms above).
   if (warp == 0 && lane < M) {
     const uint16_t* qrow = (CH ? q_nope_c : p.q_nope) + lane * p.q_nope_ts + h * p.q_nope_hs;
 #pragma unroll

@@ -221,15 +221,16 @@ __global__ void __launch_bounds__(32 * TS * kWMaxTilesPerCta, 2) mlaqp_query_war
 
   // 2. Warm L2 with the head's q rows (L2 is the coherence point, so a line
   //    fetched before the producer writes it is updated by that write; the
-  //    values are read only after the dependency wait): each q_nope row as
-  //    one bulk prefetch by the TMA unit (16-byte aligned: the host checks
-  //    the base and the strides; measured 0.06-0.07 us per layer call faster
-  //    at H = 16, M = 32 than a prefetch per 128-byte line), the 4-byte
-  //    aligned q_pe row per line.  MXFP8:
-  //    this lane's scale bytes (rows k = lane + 32i; the tile's 16 columns
-  //    share one 32-column scale block).
+  //    values are read only after the dependency wait), one prefetch per
+  //    128-byte line.  (One bulk TMA-unit prefetch per q_nope row measured
+  //    0.06-0.07 us per layer call faster at H = 16, M = 32 in a chain of
+  //    this op, but 0.4-0.7 us slower behind a producer that has just
+  //    written q.)  MXFP8: this lane's scale bytes (rows k = lane + 32i; the
+  //    tile's 16 columns share one 32-column scale block).
   if (warp == 0 && lane < M) {
-    prefetch_l2_bulk(p.q_nope + lane * p.q_nope_ts + h * p.q_nope_hs, K * 2);
+    const uint16_t* qrow = p.q_nope + lane * p.q_nope_ts + h * p.q_nope_hs;
+#pragma unroll
+    for (int o = 0; o < K; o += 64) prefetch_l2(qrow + o);
     prefetch_l2(p.q_pe + lane * p.q_pe_ts + h * p.q_pe_hs);
   }
   uint32_t sc[K / 32];
