@@ -67,3 +67,22 @@ def test_bench_bytes_match_oracle_count(M):
         assert bench.algorithmic_bytes(M, fmt, od) == oracle.algorithmic_bytes(M, 16, fmt, od)
     for fmt, _ in bench.V_FORMATS:
         assert bench.v_up_algorithmic_bytes(M, fmt) == oracle.v_up_algorithmic_bytes(M, 16, fmt)
+
+
+def test_committed_traffic_table_is_consistent():
+    # The roofline's `traffic` comes from the committed ncu table while the
+    # kernel sources still hash to the value recorded in it.  When they do,
+    # the table must cover every (pair, M) the bench times, and each launch's
+    # DRAM bytes must sit near the algorithmic reads (weights, scales and q;
+    # the output stays in L2 within the launch).
+    import bench
+    table = bench.measured_traffic()
+    if table is None:
+        pytest.skip("the kernel sources changed since the committed ncu capture")
+    for fmt, od in bench.FORMATS:
+        key = f"{fmt}->{od}"
+        for M in bench.M_POINTS:
+            assert (key, M) in table, (key, M)
+            out_bytes = M * 16 * 576 * (2 if od == "bf16" else 1)
+            reads = bench.algorithmic_bytes(M, fmt, od) - out_bytes
+            assert 0.98 * reads <= table[(key, M)] <= 1.05 * reads, (key, M, table[(key, M)], reads)
